@@ -1,0 +1,443 @@
+// capi.cpp -- the extern "C" boundary: plans, runs, status, cache queries.
+//
+// A plan holds the validated problem, its tile configuration, a 4-byte device
+// status word (device-side timeouts), an optional staging workspace, and a
+// small cache of TMA descriptors keyed by the operand pointers of the last
+// run.  gemm_run encodes descriptors only when the pointers change, stages
+// misaligned operands, and launches the chosen kernel on the caller's stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <unordered_set>
+
+#include "dispatch.h"
+#include "gemm13.h"
+#include "internal.h"
+
+using namespace g13;
+
+namespace {
+
+constexpr uint64_t kPlanMagic = 0x67656d6d31335f70ull;  // "gemm13_p"
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = []() -> EncodeTiledFn {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+bool log_enabled() {
+    static const bool on = [] {
+        const char* v = std::getenv("GEMM_LOG");
+        return v && v[0] && v[0] != '0';
+    }();
+    return on;
+}
+
+}  // namespace
+
+struct gemm_plan_s {
+    uint64_t magic = kPlanMagic;
+    Problem p{};
+    gemm_config_t cfg{};
+    int device = 0;
+    int num_sms = 0;
+    bool cache_hit = false;
+    unsigned* d_status = nullptr;
+    void* d_ws = nullptr;
+    size_t ws_bytes = 0;
+    size_t ws_b_off = 0;
+    int64_t lda_s = 0, ldb_s = 0;        // leading dims of the staged copies
+    int64_t stride_as = 0, stride_bs = 0;
+    std::mutex mu;                        // guards the descriptor cache
+    const void* mapA_src = nullptr;
+    const void* mapB_src = nullptr;
+    CUtensorMap mapA{}, mapB{};
+};
+
+namespace {
+
+std::mutex g_live_mu;
+std::unordered_set<const gemm_plan_s*> g_live;
+
+bool plan_alive(const gemm_plan_s* p) {
+    if (!p) return false;
+    std::lock_guard<std::mutex> lk(g_live_mu);
+    return g_live.count(p) != 0;
+}
+
+int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+
+// Staged copy geometry for one operand: rows x cols per batch entry.
+struct OperandGeom {
+    int64_t rows, cols, ld, bstride, batches;  // batches = 1 if shared
+};
+
+OperandGeom geom_a(const Problem& p) {
+    const int64_t bt = p.epi.batch;
+    const bool shared = bt == 1 || p.epi.stride_a == 0;
+    return {p.M, p.K, p.lda, p.epi.stride_a, shared ? 1 : bt};
+}
+
+OperandGeom geom_b(const Problem& p) {
+    const int64_t bt = p.epi.batch;
+    const bool shared = bt == 1 || p.epi.stride_b == 0;
+    const bool kn = p.epi.b_layout == GEMM_B_KN;
+    return {kn ? p.K : p.N, kn ? p.N : p.K, p.ldb, p.epi.stride_b, shared ? 1 : bt};
+}
+
+int map_cuda_error(cudaError_t e) {
+    if (e == cudaSuccess) return GEMM_OK;
+    if (e == cudaErrorMemoryAllocation) return GEMM_ERR_OUT_OF_MEMORY;
+    if (e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver ||
+        e == cudaErrorNoKernelImageForDevice)
+        return GEMM_ERR_NO_DEVICE;
+    return GEMM_ERR_CUDA;
+}
+
+// Encodes a 3-D tiled descriptor: dims innermost first (cols, rows, batches).
+int encode(CUtensorMap* m, int dtype, const void* base, int64_t cols, int64_t rows, int64_t ld,
+           int64_t batches, int64_t bstride, uint32_t box_cols, uint32_t box_rows,
+           CUtensorMapSwizzle swz) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return GEMM_ERR_NO_DEVICE;
+    const int esz = dtype_size(dtype);
+    CUtensorMapDataType t = dtype == GEMM_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                            : dtype == GEMM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(batches)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * esz),
+                             static_cast<cuuint64_t>((batches > 1 ? bstride : rows * ld) * esz)};
+    if (strides[1] == 0) strides[1] = strides[0];
+    cuuint32_t box[3] = {box_cols, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, t, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+int kernels_per_run(const gemm_plan_s* pl) {
+    const Problem& p = pl->p;
+    if (p.M == 0 || p.N == 0) return 0;
+    if (pl->cfg.kernel == GEMM_KERNEL_SKINNY) return 1;
+    return 1 + (pl->cfg.stage_a ? 1 : 0) + (pl->cfg.stage_b ? 1 : 0);
+}
+
+int make_plan(const Problem& p, const gemm_config_t* forced, gemm_plan_t* out_plan) {
+    int dev = 0;
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce != cudaSuccess) return GEMM_ERR_NO_DEVICE;
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return GEMM_ERR_NO_DEVICE;
+    if (major != 10 || minor != 3) return GEMM_ERR_NO_DEVICE;
+
+    gemm_config_t cfg;
+    bool hit = false;
+    int rc = forced ? check_config(p, *forced, &cfg) : cached_config(p, sms, &cfg, &hit);
+    if (rc != GEMM_OK) return rc;
+    if (cfg.kernel == GEMM_KERNEL_TC && tc_smem_bytes(cfg) == 0) return GEMM_ERR_UNSUPPORTED;
+    if (cfg.kernel == GEMM_KERNEL_FFMA && ffma_smem_bytes(cfg) == 0) return GEMM_ERR_UNSUPPORTED;
+
+    gemm_plan_s* pl = new (std::nothrow) gemm_plan_s();
+    if (!pl) return GEMM_ERR_OUT_OF_MEMORY;
+    pl->p = p;
+    pl->cfg = cfg;
+    pl->device = dev;
+    pl->num_sms = sms;
+    pl->cache_hit = hit;
+
+    // Staging workspace: aligned, row-padded copies of misaligned operands.
+    const int esz = dtype_size(p.dtype);
+    const int64_t pad = 16 / esz;
+    size_t ws = 0;
+    if (cfg.stage_a) {
+        const OperandGeom g = geom_a(p);
+        pl->lda_s = round_up(std::max<int64_t>(g.cols, 1), pad);
+        pl->stride_as = g.rows * pl->lda_s;
+        ws += static_cast<size_t>(round_up(g.batches * pl->stride_as * esz, 256));
+    }
+    pl->ws_b_off = ws;
+    if (cfg.stage_b) {
+        const OperandGeom g = geom_b(p);
+        pl->ldb_s = round_up(std::max<int64_t>(g.cols, 1), pad);
+        pl->stride_bs = g.rows * pl->ldb_s;
+        ws += static_cast<size_t>(round_up(g.batches * pl->stride_bs * esz, 256));
+    }
+    ce = cudaMalloc(reinterpret_cast<void**>(&pl->d_status), sizeof(unsigned));
+    if (ce == cudaSuccess) ce = cudaMemset(pl->d_status, 0, sizeof(unsigned));
+    if (ce == cudaSuccess && ws > 0) ce = cudaMalloc(&pl->d_ws, ws);
+    if (ce != cudaSuccess) {
+        if (pl->d_status) cudaFree(pl->d_status);
+        delete pl;
+        return map_cuda_error(ce);
+    }
+    pl->ws_bytes = ws;
+    {
+        std::lock_guard<std::mutex> lk(g_live_mu);
+        g_live.insert(pl);
+    }
+    if (log_enabled())
+        std::fprintf(stderr,
+                     "[gemm13] plan dtype=%d M=%lld N=%lld K=%lld batch=%lld layout=%s -> "
+                     "kernel=%d tile=%dx%dx%d stages=%d raster=%d stage_a=%d stage_b=%d "
+                     "ws=%zu cache=%s\n",
+                     p.dtype, (long long)p.M, (long long)p.N, (long long)p.K,
+                     (long long)p.epi.batch, p.epi.b_layout == GEMM_B_KN ? "KN" : "NK", cfg.kernel,
+                     cfg.bm, cfg.bn, cfg.bk, cfg.stages, cfg.raster_group, cfg.stage_a, cfg.stage_b,
+                     ws, forced ? "forced" : (hit ? "hit" : "miss"));
+    *out_plan = pl;
+    return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void gemm_epilogue_init(gemm_epilogue_t* e) {
+    if (!e) return;
+    std::memset(e, 0, sizeof(*e));
+    e->b_layout = GEMM_B_KN;
+    e->out_dtype = GEMM_F32;
+    e->act = GEMM_ACT_NONE;
+    e->beta = 1.0f;
+    e->batch = 1;
+}
+
+int gemm_plan(gemm_dtype_t dtype, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+              int64_t ldc, const gemm_epilogue_t* epilogue, gemm_plan_t* out_plan) {
+    if (!out_plan) return GEMM_ERR_INVALID_ARG;
+    *out_plan = nullptr;
+    Problem p;
+    const int rc = make_problem(dtype, M, N, K, lda, ldb, ldc, epilogue, &p);
+    if (rc != GEMM_OK) return rc;
+    return make_plan(p, nullptr, out_plan);
+}
+
+int gemm_plan_with_config(gemm_dtype_t dtype, int64_t M, int64_t N, int64_t K, int64_t lda,
+                          int64_t ldb, int64_t ldc, const gemm_epilogue_t* epilogue,
+                          const gemm_config_t* cfg, gemm_plan_t* out_plan) {
+    if (!out_plan || !cfg) return GEMM_ERR_INVALID_ARG;
+    *out_plan = nullptr;
+    if (cfg->kernel == GEMM_KERNEL_AUTO) return GEMM_ERR_INVALID_ARG;
+    Problem p;
+    const int rc = make_problem(dtype, M, N, K, lda, ldb, ldc, epilogue, &p);
+    if (rc != GEMM_OK) return rc;
+    return make_plan(p, cfg, out_plan);
+}
+
+int gemm_run(gemm_plan_t plan, const void* A, const void* B, void* C, const void* bias,
+             const void* residual, float alpha, void* stream) {
+    if (!plan_alive(plan)) return GEMM_ERR_BAD_PLAN;
+    const Problem& p = plan->p;
+    const gemm_epilogue_t& ep = p.epi;
+    if (p.M == 0 || p.N == 0) return GEMM_OK;
+    if (!C) return GEMM_ERR_INVALID_ARG;
+    if (p.K > 0 && (!A || !B)) return GEMM_ERR_INVALID_ARG;
+    if ((ep.has_bias != 0) != (bias != nullptr)) return GEMM_ERR_INVALID_ARG;
+    if ((ep.has_residual != 0) != (residual != nullptr)) return GEMM_ERR_INVALID_ARG;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != plan->device) return GEMM_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int esz = dtype_size(p.dtype);
+    const int osz = dtype_size(ep.out_dtype);
+
+    EpiParams e{};
+    e.C = C;
+    e.ldc = p.ldc;
+    e.stride_c = ep.batch > 1 ? ep.stride_c : 0;
+    e.bias = static_cast<const float*>(bias);
+    e.R = static_cast<const float*>(residual);
+    e.ldr = ep.ldr;
+    e.stride_r = ep.batch > 1 ? ep.stride_r : 0;
+    e.M = p.M;
+    e.N = p.N;
+    e.alpha = alpha;
+    e.beta = ep.beta;
+    e.out_dtype = ep.out_dtype;
+    e.act = ep.act;
+    const uintptr_t cvec_bytes = static_cast<uintptr_t>(4 * osz);
+    e.c_vec = (reinterpret_cast<uintptr_t>(C) % cvec_bytes == 0) && ((p.ldc * osz) % cvec_bytes == 0) &&
+              (ep.batch == 1 || (e.stride_c * osz) % cvec_bytes == 0);
+    e.r_vec = residual && (reinterpret_cast<uintptr_t>(residual) % 16 == 0) && (ep.ldr % 4 == 0) &&
+              (ep.batch == 1 || e.stride_r % 4 == 0);
+
+    LaunchCtx lc{};
+    lc.status = plan->d_status;
+    lc.timeout_ns = static_cast<uint64_t>(ep.timeout_ms) * 1000000ull;
+    lc.flags = ep.flags;
+    lc.num_sms = plan->num_sms;
+    lc.stream = st;
+
+    Shape s{p.M, p.N, p.K, ep.batch, 1, 1};
+    const gemm_config_t& cfg = plan->cfg;
+    cudaError_t ce;
+
+    if (cfg.kernel == GEMM_KERNEL_SKINNY) {
+        SkinnyArgs a{};
+        a.A = A;
+        a.B = B;
+        a.lda = p.lda;
+        a.ldb = p.ldb;
+        a.stride_a = ep.batch > 1 ? ep.stride_a : 0;
+        a.stride_b = ep.batch > 1 ? ep.stride_b : 0;
+        a.dtype = p.dtype;
+        a.b_layout = ep.b_layout;
+        ce = launch_skinny(cfg, a, s, e, lc);
+        return map_cuda_error(ce);
+    }
+
+    // Effective (possibly staged) operands for the TMA kernels.
+    const OperandGeom ga = geom_a(p), gb = geom_b(p);
+    const void* a_src = A;
+    const void* b_src = B;
+    int64_t lda = p.lda, ldb = p.ldb;
+    int64_t sa = ga.bstride, sb = gb.bstride;
+    if (reinterpret_cast<uintptr_t>(A) % 16 != 0 && !cfg.stage_a) return GEMM_ERR_MISALIGNED;
+    if (reinterpret_cast<uintptr_t>(B) % 16 != 0 && !cfg.stage_b) return GEMM_ERR_MISALIGNED;
+    if (cfg.stage_a) {
+        ce = launch_stage_copy(A, ga.rows, ga.cols, ga.ld, ga.bstride, ga.batches, esz, plan->d_ws,
+                               plan->lda_s, st);
+        if (ce != cudaSuccess) return map_cuda_error(ce);
+        a_src = plan->d_ws;
+        lda = plan->lda_s;
+        sa = plan->stride_as;
+    }
+    if (cfg.stage_b) {
+        void* dst = static_cast<char*>(plan->d_ws) + plan->ws_b_off;
+        ce = launch_stage_copy(B, gb.rows, gb.cols, gb.ld, gb.bstride, gb.batches, esz, dst,
+                               plan->ldb_s, st);
+        if (ce != cudaSuccess) return map_cuda_error(ce);
+        b_src = dst;
+        ldb = plan->ldb_s;
+        sb = plan->stride_bs;
+    }
+    s.a_bmul = ga.batches > 1 ? 1 : 0;
+    s.b_bmul = gb.batches > 1 ? 1 : 0;
+
+    CUtensorMap mA, mB;
+    {
+        std::lock_guard<std::mutex> lk(plan->mu);
+        if (plan->mapA_src != a_src || plan->mapB_src != b_src) {
+            const bool kn = ep.b_layout == GEMM_B_KN;
+            int rc;
+            if (cfg.kernel == GEMM_KERNEL_TC) {
+                rc = encode(&plan->mapA, p.dtype, a_src, ga.cols, ga.rows, lda, ga.batches, sa, 64,
+                            128, CU_TENSOR_MAP_SWIZZLE_128B);
+                if (rc == GEMM_OK)
+                    rc = encode(&plan->mapB, p.dtype, b_src, gb.cols, gb.rows, ldb, gb.batches, sb,
+                                64, kn ? 64 : static_cast<uint32_t>(cfg.bn),
+                                CU_TENSOR_MAP_SWIZZLE_128B);
+            } else {
+                rc = encode(&plan->mapA, p.dtype, a_src, ga.cols, ga.rows, lda, ga.batches, sa, 32,
+                            128, CU_TENSOR_MAP_SWIZZLE_128B);
+                if (rc == GEMM_OK)
+                    rc = kn ? encode(&plan->mapB, p.dtype, b_src, gb.cols, gb.rows, ldb, gb.batches,
+                                     sb, 128, 32, CU_TENSOR_MAP_SWIZZLE_NONE)
+                            : encode(&plan->mapB, p.dtype, b_src, gb.cols, gb.rows, ldb, gb.batches,
+                                     sb, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+            }
+            if (rc != GEMM_OK) {
+                plan->mapA_src = plan->mapB_src = nullptr;
+                return rc;
+            }
+            plan->mapA_src = a_src;
+            plan->mapB_src = b_src;
+        }
+        mA = plan->mapA;
+        mB = plan->mapB;
+    }
+    if (cfg.kernel == GEMM_KERNEL_TC)
+        ce = launch_tc(cfg, p.dtype, ep.b_layout, mA, mB, s, e, lc);
+    else
+        ce = launch_ffma(cfg, ep.b_layout, mA, mB, s, e, lc);
+    return map_cuda_error(ce);
+}
+
+int gemm_plan_status(gemm_plan_t plan) {
+    if (!plan_alive(plan)) return GEMM_ERR_BAD_PLAN;
+    if (cudaDeviceSynchronize() != cudaSuccess) return GEMM_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpy(&v, plan->d_status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    return (v & 1u) ? GEMM_ERR_DEVICE_TIMEOUT : GEMM_OK;
+}
+
+int gemm_plan_info(gemm_plan_t plan, gemm_plan_info_t* out) {
+    if (!plan_alive(plan)) return GEMM_ERR_BAD_PLAN;
+    if (!out) return GEMM_ERR_INVALID_ARG;
+    out->config = plan->cfg;
+    out->workspace_bytes = static_cast<int64_t>(plan->ws_bytes);
+    out->num_sms = plan->num_sms;
+    out->device = plan->device;
+    out->cache_hit = plan->cache_hit ? 1 : 0;
+    out->kernels_per_run = kernels_per_run(plan);
+    return GEMM_OK;
+}
+
+void gemm_plan_destroy(gemm_plan_t plan) {
+    {
+        std::lock_guard<std::mutex> lk(g_live_mu);
+        if (!plan || !g_live.erase(plan)) return;
+    }
+    if (plan->d_status) cudaFree(plan->d_status);
+    if (plan->d_ws) cudaFree(plan->d_ws);
+    plan->magic = 0;
+    delete plan;
+}
+
+int gemm_select_config(gemm_dtype_t dtype, int64_t M, int64_t N, int64_t K, int64_t lda,
+                       int64_t ldb, int64_t ldc, const gemm_epilogue_t* epilogue, int32_t num_sms,
+                       gemm_config_t* out) {
+    if (!out) return GEMM_ERR_INVALID_ARG;
+    Problem p;
+    const int rc = make_problem(dtype, M, N, K, lda, ldb, ldc, epilogue, &p);
+    if (rc != GEMM_OK) return rc;
+    return choose_config(p, num_sms, out);
+}
+
+void gemm_cache_stats(int64_t* entries, int64_t* hits, int64_t* misses) {
+    cache_stats(entries, hits, misses);
+}
+
+void gemm_cache_clear(void) { cache_clear(); }
+
+const char* gemm_strerror(int status) {
+    switch (status) {
+        case GEMM_OK: return "ok";
+        case GEMM_ERR_INVALID_ARG: return "invalid argument";
+        case GEMM_ERR_UNSUPPORTED: return "unsupported configuration";
+        case GEMM_ERR_MISALIGNED: return "operand base pointer not 16-byte aligned for this plan";
+        case GEMM_ERR_CUDA: return "CUDA call failed";
+        case GEMM_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+        case GEMM_ERR_BAD_PLAN: return "invalid or destroyed plan";
+        case GEMM_ERR_NO_DEVICE: return "no usable sm_103 CUDA device";
+        case GEMM_ERR_OUT_OF_MEMORY: return "device allocation failed";
+        default: return "unknown status";
+    }
+}
+
+const char* gemm_version(void) { return "gemm13 0.1.0 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,222 @@
+// dispatch.cpp -- validation, shape buckets and the configuration cache.
+//
+// "DeepGEMM", sec. 2.3 and 4.3: choose tile parameters per problem size,
+// hit a cached configuration when the same shape comes back, and switch to a
+// small-block kernel when M or N is small.  Buckets here:
+//   * empty problems (M or N = 0) and K = 0, and M or N <= kSkinnyMax:
+//     the memory-bound skinny kernel;
+//   * FP32 inputs: the FFMA kernel, 128x128x32 tiles;
+//   * FP16/BF16 inputs: the tcgen05 kernel, 128 x BN x 64 tiles, BN chosen
+//     between 128 and 256 by the number of waves the tile count needs on
+//     the device's SMs (each wave costs time proportional to BN).
+// Operands whose strides rule out TMA are staged into an aligned copy.
+#include "dispatch.h"
+
+#include <algorithm>
+#include <array>
+#include <map>
+#include <mutex>
+
+namespace g13 {
+
+namespace {
+constexpr int64_t kSkinnyMax = 8;
+
+std::mutex g_cache_mu;
+std::map<std::array<int64_t, 19>, gemm_config_t> g_cache;
+int64_t g_hits = 0, g_misses = 0;
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+}  // namespace
+
+int dtype_size(int dtype) {
+    switch (dtype) {
+        case GEMM_F32: return 4;
+        case GEMM_F16:
+        case GEMM_BF16: return 2;
+        default: return 0;
+    }
+}
+
+int make_problem(gemm_dtype_t dtype, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                 int64_t ldc, const gemm_epilogue_t* epi, Problem* p) {
+    if (!p) return GEMM_ERR_INVALID_ARG;
+    gemm_epilogue_t e;
+    gemm_epilogue_init(&e);
+    if (epi) e = *epi;
+    if (dtype_size(dtype) == 0) return GEMM_ERR_INVALID_ARG;
+    if (e.out_dtype != GEMM_F32 && e.out_dtype != GEMM_BF16 && e.out_dtype != GEMM_F16)
+        return GEMM_ERR_INVALID_ARG;
+    if (e.b_layout != GEMM_B_KN && e.b_layout != GEMM_B_NK) return GEMM_ERR_INVALID_ARG;
+    if (e.act != GEMM_ACT_NONE && e.act != GEMM_ACT_GELU_ERF && e.act != GEMM_ACT_RELU)
+        return GEMM_ERR_INVALID_ARG;
+    if (e.has_bias != 0 && e.has_bias != 1) return GEMM_ERR_INVALID_ARG;
+    if (e.has_residual != 0 && e.has_residual != 1) return GEMM_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+    // Sizes must fit the 32-bit coordinates of TMA boxes.
+    if (M > (int64_t(1) << 31) - 256 || N > (int64_t(1) << 31) - 256 ||
+        K > (int64_t(1) << 31) - 256)
+        return GEMM_ERR_UNSUPPORTED;
+    if (e.batch == 0) e.batch = 1;
+    if (e.batch < 0 || e.batch > (int64_t(1) << 31) - 1) return GEMM_ERR_INVALID_ARG;
+    if (lda < std::max<int64_t>(K, 1)) return GEMM_ERR_INVALID_ARG;
+    const int64_t ldb_min = e.b_layout == GEMM_B_KN ? N : K;
+    if (ldb < std::max<int64_t>(ldb_min, 1)) return GEMM_ERR_INVALID_ARG;
+    if (ldc < std::max<int64_t>(N, 1)) return GEMM_ERR_INVALID_ARG;
+    if (e.ldr == 0) e.ldr = ldc;
+    if (e.has_residual && e.ldr < std::max<int64_t>(N, 1)) return GEMM_ERR_INVALID_ARG;
+    if (e.stride_a < 0 || e.stride_b < 0 || e.stride_c < 0 || e.stride_r < 0)
+        return GEMM_ERR_INVALID_ARG;
+    if (e.batch > 1 && M > 0 && N > 0 && e.stride_c < M * ldc) return GEMM_ERR_INVALID_ARG;
+    if (e.timeout_ms == 0) e.timeout_ms = 2000;
+    p->dtype = dtype;
+    p->M = M;
+    p->N = N;
+    p->K = K;
+    p->lda = lda;
+    p->ldb = ldb;
+    p->ldc = ldc;
+    p->epi = e;
+    return GEMM_OK;
+}
+
+bool stride_tma_ok(int64_t ld, int64_t bstride, int64_t batch, int esz) {
+    if ((ld * esz) % 16 != 0) return false;
+    if (batch > 1 && bstride != 0 && (bstride * esz) % 16 != 0) return false;
+    return true;
+}
+
+static void set_staging(const Problem& p, gemm_config_t* c) {
+    const int esz = dtype_size(p.dtype);
+    const int64_t bt = p.epi.batch;
+    if (!stride_tma_ok(p.lda, p.epi.stride_a, bt, esz)) c->stage_a = 1;
+    if (!stride_tma_ok(p.ldb, p.epi.stride_b, bt, esz)) c->stage_b = 1;
+}
+
+int choose_config(const Problem& p, int num_sms, gemm_config_t* out) {
+    if (!out) return GEMM_ERR_INVALID_ARG;
+    if (num_sms <= 0) num_sms = 1;
+    gemm_config_t c{};
+    c.split_k = 1;
+    c.num_ctas = 0;
+    const int64_t M = p.M, N = p.N, K = p.K, bt = p.epi.batch;
+    if (M == 0 || N == 0 || K == 0 || std::min(M, N) <= kSkinnyMax) {
+        c.kernel = GEMM_KERNEL_SKINNY;
+        c.bm = 1;
+        c.bn = 1;
+        c.bk = 32;
+        c.stages = 1;
+        c.raster_group = 1;
+        *out = c;
+        return GEMM_OK;
+    }
+    if (p.dtype == GEMM_F32) {
+        c.kernel = GEMM_KERNEL_FFMA;
+        c.bm = 128;
+        c.bn = 128;
+        c.bk = 32;
+        c.stages = 3;
+        c.raster_group = 8;
+    } else {
+        c.kernel = GEMM_KERNEL_TC;
+        c.bm = 128;
+        c.bk = 64;
+        const int64_t mt = cdiv(M, 128);
+        const int64_t waves256 = cdiv(bt * mt * cdiv(N, 256), num_sms);
+        const int64_t waves128 = cdiv(bt * mt * cdiv(N, 128), num_sms);
+        // Time per wave ~ BN / efficiency.  A 128x128x16 MMA reads 8 KB of
+        // shared memory per 64 tensor-core clocks (the whole 128 B/clk), a
+        // 128x256x16 one 12 KB per 128 clocks, so 128-wide tiles run at
+        // roughly 4/5 of the 256-wide rate.
+        if (waves128 * 128 * 5 < waves256 * 256 * 4) {
+            c.bn = 128;
+            c.stages = 6;
+        } else {
+            c.bn = 256;
+            c.stages = 4;
+        }
+        c.raster_group = static_cast<int32_t>(std::min<int64_t>(16, mt));
+    }
+    set_staging(p, &c);
+    *out = c;
+    return GEMM_OK;
+}
+
+int check_config(const Problem& p, const gemm_config_t& in, gemm_config_t* out) {
+    gemm_config_t c = in;
+    if (c.split_k == 0) c.split_k = 1;
+    if (c.split_k != 1) return GEMM_ERR_UNSUPPORTED;
+    if (c.num_ctas < 0 || c.raster_group < 0) return GEMM_ERR_INVALID_ARG;
+    switch (c.kernel) {
+        case GEMM_KERNEL_SKINNY:
+            c.stage_a = c.stage_b = 0;
+            break;
+        case GEMM_KERNEL_FFMA:
+            if (p.dtype != GEMM_F32 || p.K == 0) return GEMM_ERR_UNSUPPORTED;
+            if (c.bm != 128 || c.bn != 128 || c.bk != 32) return GEMM_ERR_UNSUPPORTED;
+            if (c.stages < 2 || c.stages > 4) return GEMM_ERR_UNSUPPORTED;
+            if (c.raster_group == 0) c.raster_group = 8;
+            break;
+        case GEMM_KERNEL_TC:
+            if (p.dtype == GEMM_F32 || p.K == 0) return GEMM_ERR_UNSUPPORTED;
+            if (c.bm != 128 || c.bk != 64) return GEMM_ERR_UNSUPPORTED;
+            if (!((c.bn == 256 && (c.stages == 4 || c.stages == 3)) ||
+                  (c.bn == 128 && (c.stages == 6 || c.stages == 4))))
+                return GEMM_ERR_UNSUPPORTED;
+            if (c.raster_group == 0) c.raster_group = 16;
+            break;
+        default:
+            return GEMM_ERR_INVALID_ARG;
+    }
+    if (c.kernel != GEMM_KERNEL_SKINNY) {
+        gemm_config_t need = c;
+        need.stage_a = need.stage_b = 0;
+        set_staging(p, &need);
+        c.stage_a = (c.stage_a || need.stage_a) ? 1 : 0;
+        c.stage_b = (c.stage_b || need.stage_b) ? 1 : 0;
+    }
+    *out = c;
+    return GEMM_OK;
+}
+
+int cached_config(const Problem& p, int num_sms, gemm_config_t* out, bool* hit) {
+    const gemm_epilogue_t& e = p.epi;
+    const std::array<int64_t, 19> key = {
+        p.dtype,   p.M,        p.N,        p.K,        p.lda,        p.ldb,   p.ldc,
+        e.b_layout, e.out_dtype, e.has_bias, e.act,    e.has_residual, e.ldr, e.batch,
+        e.stride_a, e.stride_b, e.stride_c, e.stride_r, num_sms};
+    {
+        std::lock_guard<std::mutex> lk(g_cache_mu);
+        auto it = g_cache.find(key);
+        if (it != g_cache.end()) {
+            ++g_hits;
+            *out = it->second;
+            if (hit) *hit = true;
+            return GEMM_OK;
+        }
+    }
+    gemm_config_t c;
+    const int rc = choose_config(p, num_sms, &c);
+    if (rc != GEMM_OK) return rc;
+    std::lock_guard<std::mutex> lk(g_cache_mu);
+    ++g_misses;
+    g_cache.emplace(key, c);
+    *out = c;
+    if (hit) *hit = false;
+    return GEMM_OK;
+}
+
+void cache_stats(int64_t* entries, int64_t* hits, int64_t* misses) {
+    std::lock_guard<std::mutex> lk(g_cache_mu);
+    if (entries) *entries = static_cast<int64_t>(g_cache.size());
+    if (hits) *hits = g_hits;
+    if (misses) *misses = g_misses;
+}
+
+void cache_clear() {
+    std::lock_guard<std::mutex> lk(g_cache_mu);
+    g_cache.clear();
+    g_hits = g_misses = 0;
+}
+
+}  // namespace g13

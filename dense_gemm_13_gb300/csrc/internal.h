@@ -1,0 +1,72 @@
+// internal.h -- declarations shared between the host side (plan, dispatch,
+// C ABI) and the kernel translation units.  Not part of the public ABI.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "gemm13.h"
+
+namespace g13 {
+
+// Everything the fused epilogue needs: y = alpha*acc (+bias[n]) -> act -> (+beta*R) -> cast.
+struct EpiParams {
+    void* C;
+    int64_t ldc, stride_c;
+    const float* bias;
+    const float* R;
+    int64_t ldr, stride_r;
+    int64_t M, N;
+    float alpha, beta;
+    int out_dtype;   // gemm_dtype_t
+    int act;         // gemm_act_t
+    int c_vec;       // 1: C rows take aligned vector stores at columns that are multiples of 4
+    int r_vec;       // 1: R rows take aligned float4 loads at columns that are multiples of 4
+};
+
+struct Shape {
+    int64_t M, N, K, batch;
+    int a_bmul, b_bmul;  // 1, or 0 when that operand is shared by every batch entry
+};
+
+struct LaunchCtx {
+    unsigned* status;     // per-plan device status word
+    uint64_t timeout_ns;  // bound on every mbarrier wait
+    uint32_t flags;       // GEMM_FLAG_*
+    int num_sms;
+    cudaStream_t stream;
+};
+
+// Tensor-core path: A [batch][M][K] 16-bit via tmA (K innermost); B via tmB:
+// NK layout -> dims (K, N, batch), KN layout -> dims (N, K, batch).
+cudaError_t launch_tc(const gemm_config_t& cfg, int dtype, int b_layout, const CUtensorMap& tmA,
+                      const CUtensorMap& tmB, const Shape& s, const EpiParams& e,
+                      const LaunchCtx& lc);
+// Shared memory the TC kernel needs for a config (bytes), or 0 if unsupported.
+size_t tc_smem_bytes(const gemm_config_t& cfg);
+
+// FP32 FFMA path: A via tmA (dims K, M, batch), B via tmB (KN: N, K, batch; NK: K, N, batch).
+cudaError_t launch_ffma(const gemm_config_t& cfg, int b_layout, const CUtensorMap& tmA,
+                        const CUtensorMap& tmB, const Shape& s, const EpiParams& e,
+                        const LaunchCtx& lc);
+size_t ffma_smem_bytes(const gemm_config_t& cfg);
+
+// Memory-bound path for small M or N: plain (unaligned-capable) loads.
+struct SkinnyArgs {
+    const void* A;
+    const void* B;
+    int64_t lda, ldb, stride_a, stride_b;
+    int dtype;
+    int b_layout;
+};
+cudaError_t launch_skinny(const gemm_config_t& cfg, const SkinnyArgs& a, const Shape& s,
+                          const EpiParams& e, const LaunchCtx& lc);
+
+// Copies [batch][rows][cols] (row stride ld, batch stride bstride, element
+// size esz) into a dense [batch][rows][dst_ld] buffer.  Padding columns are
+// left untouched.
+cudaError_t launch_stage_copy(const void* src, int64_t rows, int64_t cols, int64_t ld,
+                              int64_t bstride, int64_t batch, int esz, void* dst,
+                              int64_t dst_ld, cudaStream_t stream);
+
+}  // namespace g13

@@ -67,6 +67,8 @@ def _mat(a: np.ndarray):
     if a.ndim not in (2, 3):
         raise ValueError("operands must be 2-D or 3-D")
     it = a.itemsize
+    if a.size == 0:
+        return a.ctypes.data, max(a.shape[-1], 1), 0, (a.shape[0] if a.ndim == 3 else 1)
     if a.shape[-1] > 1 and a.strides[-1] != it:
         raise ValueError("last dimension must be contiguous")
     ld = a.strides[-2] // it if a.shape[-2] > 1 else a.shape[-1]

@@ -1,0 +1,229 @@
+"""GPU parity: the library (through the C ABI) against the FP64 oracle.
+
+Small problems are compared element by element in full; the full-size
+workloads on tile-boundary rows/columns (every column of the sampled rows and
+every row of the sampled columns) plus a Freivalds whole-matrix check.
+Every run also checks the NaN guard bands around C.
+"""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import dense_gemm_13_gb300 as g13
+from dense_gemm_13_gb300.inputs import WORKLOADS, Workload, matrix
+from tests.gpu_check import Run, boundary_indices
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from dense_gemm_13_gb300 import _build
+    _build.build()
+    g13.load()
+
+
+def full_check(run: Run):
+    C = run.run().result()
+    run.check(C)
+    assert run.guard_ok(), "store outside the M x N window"
+    return C
+
+
+# ---------------------------------------------------------------- exact integer cases
+# Inputs in [-4, 4]: every product and partial sum is an integer below 2^24, so
+# FP32 accumulation is exact in any order and the result must equal the oracle.
+INT_SHAPES = [(128, 128, 64), (200, 300, 130), (129, 257, 65), (17, 33, 100), (1, 50, 70),
+              (300, 7, 90), (256, 512, 1024), (64, 1000, 8), (513, 129, 200)]
+
+
+def _int_workload(dtype, layout, M, N, K):
+    return Workload(f"int_{dtype}_{layout}_{M}x{N}x{K}", dtype, M, N, K, b_layout=layout,
+                    dist_a="ints", dist_b="ints")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+@pytest.mark.parametrize("shape", INT_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_exact_integer(dtype, layout, shape):
+    w = _int_workload(dtype, layout, *shape)
+    run = Run(w)
+    C = run.run().result()
+    _, cref, _ = run.oracle()
+    assert np.array_equal(C, cref.reshape(C.shape)), (
+        f"{w.name}: {np.sum(C != cref.reshape(C.shape))} mismatches, config {run.info['config']}")
+    assert run.guard_ok()
+
+
+TC_CONFIGS = [g13.Config("tc", 128, 256, 64, 4), g13.Config("tc", 128, 256, 64, 3),
+              g13.Config("tc", 128, 128, 64, 6), g13.Config("tc", 128, 128, 64, 4)]
+
+
+@pytest.mark.parametrize("cfg", TC_CONFIGS, ids=lambda c: f"bn{c.bn}s{c.stages}")
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+def test_tc_variants_exact(cfg, dtype, layout):
+    # 3 x 3 tiles of 128 x 256 with ragged edges; 5 K blocks with a ragged tail
+    w = _int_workload(dtype, layout, 300, 600, 300)
+    run = Run(w, config=cfg)
+    C = run.run().result()
+    _, cref, _ = run.oracle()
+    assert np.array_equal(C, cref.reshape(C.shape)), f"{w.name} {cfg}"
+    assert run.guard_ok()
+    # persistent grid smaller than the tile count: each CTA walks several tiles
+    cfg2 = g13.Config(cfg.kernel, cfg.bm, cfg.bn, cfg.bk, cfg.stages, num_ctas=2)
+    run2 = Run(w, tensors=run.t, config=cfg2)
+    C2 = run2.run().result()
+    assert np.array_equal(C2, cref.reshape(C.shape)), f"{w.name} {cfg2} (2 CTAs)"
+
+
+@pytest.mark.parametrize("stages", [2, 3, 4])
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+def test_ffma_variants_exact(stages, layout):
+    w = _int_workload("f32", layout, 300, 260, 200)
+    run = Run(w, config=g13.Config("ffma", 128, 128, 32, stages))
+    C = run.run().result()
+    _, cref, _ = run.oracle()
+    assert np.array_equal(C, cref.reshape(C.shape))
+    assert run.guard_ok()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_skinny_forced_exact(dtype):
+    for layout in ("kn", "nk"):
+        w = _int_workload(dtype, layout, 70, 90, 333)
+        run = Run(w, config=g13.Config("skinny"))
+        C = run.run().result()
+        _, cref, _ = run.oracle()
+        assert np.array_equal(C, cref.reshape(C.shape))
+        assert run.guard_ok()
+
+
+# ---------------------------------------------------------------- epilogues
+EPILOGUES = [
+    dict(),
+    dict(bias=True),
+    dict(act="gelu", bias=True),
+    dict(act="relu"),
+    dict(residual=True, beta=0.5),
+    dict(residual=True, bias=True, act="gelu", beta=-1.25),
+    dict(out_dtype="bf16", bias=True, act="gelu"),
+    dict(out_dtype="f16", residual=True),
+]
+
+
+@pytest.mark.parametrize("epi", EPILOGUES, ids=lambda e: "-".join(f"{k}={v}" for k, v in e.items()) or "plain")
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+def test_epilogue_variants(epi, dtype):
+    for layout in ("kn", "nk"):
+        w = Workload(f"epi_{dtype}_{layout}", dtype, 333, 520, 200, b_layout=layout, alpha=0.75,
+                     **epi)
+        full_check(Run(w, seed=3))
+    # the skinny kernel applies the same epilogue
+    w = Workload(f"epi_{dtype}_skinny", dtype, 5, 77, 300, alpha=0.75, **epi)
+    full_check(Run(w, seed=4))
+
+
+# ---------------------------------------------------------------- named workloads
+@pytest.mark.parametrize("name", ["sgemm_256", "qkt_bf16", "qkt_f16"])
+def test_workload_full(name):
+    full_check(Run(WORKLOADS[name]))
+
+
+@pytest.mark.parametrize("name", ["sgemm_4096", "bf16_4096", "bf16_8192", "ffn1_bf16", "ffn1_f16",
+                                  "ffn2_bf16", "ffn2_f16"])
+def test_workload_sampled(name):
+    w = WORKLOADS[name]
+    run = Run(w)
+    C = run.run().result()
+    rows = boundary_indices(w.M, extra=4)
+    cols = boundary_indices(w.N, extra=4)
+    run.check(C, rows=rows, label=" [sampled rows]")
+    run.check(C, cols=cols, label=" [sampled cols]")
+    if w.act == "none" and w.out_dtype == "f32":
+        run.freivalds(C)
+    assert run.guard_ok()
+    # run-to-run determinism: same inputs, same bits
+    C2 = run.run().result()
+    assert np.array_equal(C, C2), "result changed between identical runs"
+
+
+# ---------------------------------------------------------------- edge cases
+def test_empty_problems_touch_nothing():
+    for M, N in ((0, 64), (64, 0), (0, 0)):
+        w = Workload("empty", "bf16", M, N, 64)
+        run = Run(w)
+        run.run()
+        torch.cuda.synchronize()
+        assert run.info["kernels_per_run"] == 0
+        assert run.guard_ok()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_k_zero_gives_epilogue_of_zero(dtype):
+    w = Workload("k0", dtype, 37, 45, 0, bias=True, act="gelu", residual=True, beta=2.0)
+    full_check(Run(w))
+
+
+def test_misaligned_pointers_are_staged_or_rejected():
+    # A starts 1 element into its buffer (2-byte aligned): with aligned strides
+    # the plan has no workspace and must refuse; with K = 1001 it stages.
+    w = Workload("mis", "bf16", 256, 256, 1000)
+    with pytest.raises(g13.GemmError) as ei:
+        Run(w, a_offset=1).run()
+    assert ei.value.status == -3
+    w = Workload("mis_staged", "bf16", 256, 263, 1001)     # both row strides misaligned
+    run = Run(w, a_offset=1, b_offset=3)
+    cfg = run.info["config"]
+    assert cfg.stage_a == 1 and cfg.stage_b == 1 and run.info["workspace_bytes"] > 0
+    assert run.info["kernels_per_run"] == 3
+    full_check(run)
+    # FP32 with a misaligned stride goes through the same staging
+    w = Workload("mis_staged_f32", "f32", 130, 70, 301, b_layout="nk")
+    full_check(Run(w, a_offset=1, b_offset=2))
+
+
+def test_batched_shared_operand():
+    # one B shared by 6 batch entries (stride_b = 0), A and C batched
+    bt, M, N, K = 6, 200, 136, 72
+    A = matrix((bt, M, K), "normal", 0, "bf16")
+    B = matrix((N, K), "normal", 1, "bf16")
+    w = Workload("shared_b", "bf16", M, N, K, batch=bt, b_layout="nk")
+    run = Run(w, tensors={"A": A, "B": B, "bias": None, "R": None})
+    full_check(run)
+
+
+def test_plan_cache_hits():
+    g13.gemm_cache_clear()
+    p1 = g13.gemm_plan("bf16", 640, 640, 640, 640, 640, 640)
+    p2 = g13.gemm_plan("bf16", 640, 640, 640, 640, 640, 640)
+    assert not p1.info()["cache_hit"] and p2.info()["cache_hit"]
+    e, h, m = g13.gemm_cache_stats()
+    assert (e, h, m) == (1, 1, 1)
+
+
+def test_invariants_on_gpu():
+    # all-ones: every entry equals K exactly
+    for dtype, K in (("bf16", 6144), ("f32", 4097), ("f16", 1000)):
+        w = Workload("ones", dtype, 300, 260, K, dist_a="ones", dist_b="ones")
+        C = Run(w).run().result()
+        assert np.all(C == K), (dtype, K)
+    # identity: I @ B == B exactly (bf16 B, f32 out)
+    n, N = 384, 300
+    eye = torch.eye(n).to(torch.bfloat16)
+    B = matrix((n, N), "normal", 2, "bf16")
+    w = Workload("eye", "bf16", n, N, n)
+    C = Run(w, tensors={"A": eye, "B": B, "bias": None, "R": None}).run().result()
+    assert np.array_equal(C[0], B.double().numpy())
+    # transpose identity: (A B)^T vs B^T A^T through the library, within tolerance of each other
+    A = matrix((333, 190), "normal", 3, "bf16")
+    Bm = matrix((190, 277), "normal", 4, "bf16")
+    w1 = Workload("t1", "bf16", 333, 277, 190)
+    w2 = Workload("t2", "bf16", 277, 333, 190)
+    r1 = Run(w1, tensors={"A": A, "B": Bm, "bias": None, "R": None})
+    r2 = Run(w2, tensors={"A": Bm.t().contiguous(), "B": A.t().contiguous(), "bias": None, "R": None})
+    C1, C2 = r1.run().result()[0], r2.run().result()[0]
+    _, _, s = r1.oracle()
+    assert np.all(np.abs(C1 - C2.T) <= 2 * (2e-4 * s + 1e-6))
