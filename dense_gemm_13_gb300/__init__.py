@@ -17,7 +17,7 @@ import threading
 
 __all__ = ["Epilogue", "Config", "Plan", "GemmError", "gemm_plan", "gemm_run", "gemm_plan_status",
            "gemm_plan_info", "gemm_select_config", "gemm_cache_stats", "gemm_cache_clear",
-           "gemm_strerror", "gemm_version", "lib", "load", "matmul", "DTYPES", "ACTS", "LAYOUTS",
+           "gemm_strerror", "gemm_version", "gemm_run_noalloc", "lib", "load", "matmul", "DTYPES", "ACTS", "LAYOUTS",
            "KERNELS", "LIB_PATH"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgemm13.so")
@@ -31,7 +31,8 @@ FLAG_TEST_STALL = 0x80000000
 
 STATUS = {0: "GEMM_OK", -1: "GEMM_ERR_INVALID_ARG", -2: "GEMM_ERR_UNSUPPORTED",
           -3: "GEMM_ERR_MISALIGNED", -4: "GEMM_ERR_CUDA", -5: "GEMM_ERR_DEVICE_TIMEOUT",
-          -6: "GEMM_ERR_BAD_PLAN", -7: "GEMM_ERR_NO_DEVICE", -8: "GEMM_ERR_OUT_OF_MEMORY"}
+          -6: "GEMM_ERR_BAD_PLAN", -7: "GEMM_ERR_NO_DEVICE", -8: "GEMM_ERR_OUT_OF_MEMORY",
+          -9: "GEMM_ERR_SCRATCH_LIMIT"}
 
 
 class GemmError(RuntimeError):
@@ -108,6 +109,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.gemm_strerror.restype = ctypes.c_char_p
         L.gemm_version.argtypes = []
         L.gemm_version.restype = ctypes.c_char_p
+        L.gemm_run_noalloc.argtypes = [i32, i64, i64, i64, vp, i64, vp, i64, vp, i64,
+                                       ctypes.POINTER(_Epilogue), vp, vp, ctypes.c_float, vp]
+        L.gemm_run_noalloc.restype = i32
         if path is None:
             _lib = L
         return L
@@ -289,6 +293,27 @@ def gemm_cache_stats() -> tuple[int, int, int]:
 
 def gemm_cache_clear() -> None:
     lib().gemm_cache_clear()
+
+
+def gemm_run_noalloc(dtype: str, M: int, N: int, K: int, A, lda: int, B, ldb: int, C, ldc: int,
+                     epilogue: Epilogue | None = None, bias=None, residual=None,
+                     alpha: float = 1.0, stream=None) -> int:
+    """gemm_run_noalloc: one GEMM without any allocation (fixed in-library scratch).
+
+    For callers that cannot allocate device memory where they run the GEMM;
+    see include/gemm13.h for the scratch limit and the sharing rules.
+    """
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream().cuda_stream
+    elif not isinstance(stream, int):
+        stream = stream.cuda_stream
+    ce = (epilogue or Epilogue())._c()
+    rc = lib().gemm_run_noalloc(DTYPES[dtype], M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc,
+                                ctypes.byref(ce), _ptr(bias), _ptr(residual), float(alpha), stream)
+    if rc != 0:
+        raise GemmError(rc, "gemm_run_noalloc")
+    return rc
 
 
 _plans: dict = {}

@@ -434,6 +434,8 @@ const char* gemm_strerror(int status) {
         case GEMM_ERR_BAD_PLAN: return "invalid or destroyed plan";
         case GEMM_ERR_NO_DEVICE: return "no usable sm_103 CUDA device";
         case GEMM_ERR_OUT_OF_MEMORY: return "device allocation failed";
+        case GEMM_ERR_SCRATCH_LIMIT:
+            return "problem needs more than the 64 MiB fixed scratch of gemm_run_noalloc";
         default: return "unknown status";
     }
 }

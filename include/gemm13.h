@@ -63,7 +63,8 @@ typedef enum {
     GEMM_ERR_DEVICE_TIMEOUT = -5,/* a kernel gave up waiting on a barrier (status word) */
     GEMM_ERR_BAD_PLAN = -6,      /* NULL, destroyed or foreign plan handle */
     GEMM_ERR_NO_DEVICE = -7,     /* no usable CUDA device, or not an sm_103 device */
-    GEMM_ERR_OUT_OF_MEMORY = -8  /* plan workspace could not be allocated */
+    GEMM_ERR_OUT_OF_MEMORY = -8, /* plan workspace could not be allocated */
+    GEMM_ERR_SCRATCH_LIMIT = -9  /* gemm_run_noalloc: staged operands exceed its fixed scratch */
 } gemm_status_t;
 
 /* Plan flags (gemm_epilogue_t.flags). */
@@ -195,6 +196,41 @@ const char* gemm_strerror(int status);
 
 /* Library version string. */
 const char* gemm_version(void);
+
+/*
+ * gemm_run_noalloc -- the same GEMM as gemm_plan + gemm_run in one call that
+ * allocates no memory at all (no cudaMalloc, no plan, no host heap).  The
+ * pages have no counterpart: this exists for callers that cannot allocate
+ * device memory where they run a GEMM -- code inside an allocator or memory-
+ * pool callback, code holding a lock the allocator also takes, or programs
+ * that reserve all device memory up front.
+ *
+ * Arguments: as gemm_plan followed by gemm_run (same meaning, layout and
+ * validation; epilogue may be NULL).  A, B, C, bias and residual are the
+ * caller's device buffers; the call enqueues on `stream` and returns.
+ *
+ * Scratch: operands that TMA cannot read in place (strides or base addresses
+ * not 16-byte aligned) are copied into a fixed 64 MiB device array inside the
+ * library, one per GPU, resident from library load until process exit.  The
+ * array also holds the status word.  If the staged copies need more than
+ * that (each staged row padded to 16 bytes, 256 bytes reserved), the call
+ * returns GEMM_ERR_SCRATCH_LIMIT and does nothing.
+ *
+ * Sharing: every call on a device uses the same array and finds the previous
+ * call's data in it (it rewrites what it uses).  Calls whose work overlaps on
+ * the GPU -- on different streams or from several threads -- race on the
+ * array; order them on one stream.  Device-side wait timeouts are not
+ * reported by this call.
+ *
+ * Set-up: the first call on each device (with that device current) looks up
+ * the array's device address; make that first call before any stream capture.
+ *
+ * Errors: INVALID_ARG, UNSUPPORTED, SCRATCH_LIMIT, NO_DEVICE, CUDA.
+ */
+int gemm_run_noalloc(gemm_dtype_t dtype, int64_t M, int64_t N, int64_t K,
+                     const void* A, int64_t lda, const void* B, int64_t ldb,
+                     void* C, int64_t ldc, const gemm_epilogue_t* epilogue,
+                     const void* bias, const void* residual, float alpha, void* stream);
 
 #ifdef __cplusplus
 }
