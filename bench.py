@@ -92,24 +92,28 @@ def peaks():
             "sm_max_mhz": 2070.0}, "fallback"
 
 
-def source_hash() -> str:
+KERNEL_SOURCES = {"tc": "tc_sm103.cu", "ffma": "sgemm_ffma.cu", "skinny": "aux_kernels.cu"}
+
+
+def source_hash(kernel: str) -> str:
+    """Hash of the files that make up one kernel family (its .cu and the shared headers)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_gemm_13_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in (KERNEL_SOURCES[kernel], "epilogue.cuh", "ptx.cuh", "internal.h"):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel: str, workload: str):
-    """dram bytes per launch from a committed ncu summary, if it matches the current sources."""
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged since."""
     path = os.path.join(ROOT, "profiles", f"ncu_{kernel}_{workload}.md")
-    if not os.path.exists(path):
+    if not os.path.exists(path) or kernel not in KERNEL_SOURCES:
         return None
     txt = open(path).read()
     m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
     hsh = re.search(r"source_hash:\s*([0-9a-f]+)", txt)
-    if not m or not hsh or hsh.group(1) != source_hash():
+    if not m or not hsh or hsh.group(1) != source_hash(kernel):
         return None
     return float(m.group(1))
 
