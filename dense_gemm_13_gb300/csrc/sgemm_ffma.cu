@@ -62,6 +62,20 @@ __device__ __forceinline__ void tile_coords(int64_t t, int64_t m_tiles, int64_t 
     nt = w / gm;
 }
 
+// Two FP32 lanes in one 64-bit register pair, for the packed fma.rn.f32x2
+// (one instruction issues two FMAs, halving the issue slots the FMAs take).
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ void ffma2(uint64_t& d, uint64_t a, uint64_t b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+
 // Waits for a phase without looking at the abort flag (used to drain copies
 // already in flight before a CTA gives up).
 __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
@@ -70,7 +84,7 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, uint64
         if (globaltimer_ns() - t0 > timeout_ns) return;
 }
 
-template <int STAGES, bool B_NK>
+template <int STAGES, bool B_NK, bool PACKED>
 __global__ void __launch_bounds__(FTHREADS, 2)
     ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const FfmaArgs args) {
@@ -127,11 +141,16 @@ __global__ void __launch_bounds__(FTHREADS, 2)
 
     const int wm = warp & 3, wn = warp >> 2;
     const int lr = lane >> 3, lc = lane & 7;
+    // acc[i][j] (scalar path) or acc2[i][j/2] holding columns (j, j+1) (packed path)
     float acc[8][8];
+    uint64_t acc2[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+        for (int j = 0; j < 8; ++j) {
+            acc[i][j] = 0.0f;
+            if (j < 4) acc2[i][j] = 0ull;
+        }
 
     bool ok = true;
     int kt_done = -1;  // last K tile this thread saw complete
@@ -145,7 +164,32 @@ __global__ void __launch_bounds__(FTHREADS, 2)
         kt_done = kt;
         const float* As = reinterpret_cast<const float*>(smem + s * F_STAGE_BYTES);
         const float* Bs = reinterpret_cast<const float*>(smem + s * F_STAGE_BYTES + F_A_BYTES);
-        if (!B_NK) {
+        if (!B_NK && PACKED) {
+#pragma unroll
+            for (int kq = 0; kq < FBK / 4; ++kq) {
+                float4 a4[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int row = wm * 32 + lr + 4 * i;
+                    a4[i] = *reinterpret_cast<const float4*>(As + row * FBK +
+                                                              ((kq ^ (row & 7)) << 2));
+                }
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const float* brow = Bs + (kq * 4 + kk) * FBN + wn * 64 + lc * 4;
+                    const ulonglong2 b0 = *reinterpret_cast<const ulonglong2*>(brow);
+                    const ulonglong2 b1 = *reinterpret_cast<const ulonglong2*>(brow + 32);
+                    const uint64_t bp[4] = {b0.x, b0.y, b1.x, b1.y};
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float a = kk == 0 ? a4[i].x : kk == 1 ? a4[i].y : kk == 2 ? a4[i].z : a4[i].w;
+                        const uint64_t ap = pack2(a, a);
+#pragma unroll
+                        for (int jp = 0; jp < 4; ++jp) ffma2(acc2[i][jp], ap, bp[jp]);
+                    }
+                }
+            }
+        } else if (!B_NK) {
 #pragma unroll
             for (int kq = 0; kq < FBK / 4; ++kq) {
                 float4 a4[8];
@@ -226,6 +270,12 @@ __global__ void __launch_bounds__(FTHREADS, 2)
 
     // Fused epilogue; C written once.
     const EpiParams& e = args.e;
+    if (PACKED) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int jp = 0; jp < 4; ++jp) unpack2(acc2[i][jp], acc[i][2 * jp], acc[i][2 * jp + 1]);
+    }
     if (!B_NK) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -244,7 +294,7 @@ __global__ void __launch_bounds__(FTHREADS, 2)
     }
 }
 
-template <int STAGES, bool B_NK>
+template <int STAGES, bool B_NK, bool PACKED>
 cudaError_t launch_ffma_t(const gemm_config_t& cfg, const CUtensorMap& tmA,
                           const CUtensorMap& tmB, const Shape& s, const EpiParams& e,
                           const LaunchCtx& lc) {
@@ -260,7 +310,7 @@ cudaError_t launch_ffma_t(const gemm_config_t& cfg, const CUtensorMap& tmA,
     a.timeout_ns = lc.timeout_ns;
     a.flags = lc.flags;
     const int smem = ffma_smem_total<STAGES>();
-    auto kern = ffma_kernel<STAGES, B_NK>;
+    auto kern = ffma_kernel<STAGES, B_NK, PACKED>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     const int64_t grid = a.tiles_per_batch * s.batch;
@@ -283,15 +333,19 @@ cudaError_t launch_ffma(const gemm_config_t& cfg, int b_layout, const CUtensorMa
                         const CUtensorMap& tmB, const Shape& s, const EpiParams& e,
                         const LaunchCtx& lc) {
     const bool nk = b_layout == GEMM_B_NK;
+    const bool packed = cfg.variant == 1 && !nk;  // the packed main loop exists for KN only
+#define G13_FFMA_CASE(ST)                                                          \
+    case ST:                                                                       \
+        if (nk) return launch_ffma_t<ST, true, false>(cfg, tmA, tmB, s, e, lc);    \
+        if (packed) return launch_ffma_t<ST, false, true>(cfg, tmA, tmB, s, e, lc); \
+        return launch_ffma_t<ST, false, false>(cfg, tmA, tmB, s, e, lc);
     switch (cfg.stages) {
-        case 2: return nk ? launch_ffma_t<2, true>(cfg, tmA, tmB, s, e, lc)
-                          : launch_ffma_t<2, false>(cfg, tmA, tmB, s, e, lc);
-        case 3: return nk ? launch_ffma_t<3, true>(cfg, tmA, tmB, s, e, lc)
-                          : launch_ffma_t<3, false>(cfg, tmA, tmB, s, e, lc);
-        case 4: return nk ? launch_ffma_t<4, true>(cfg, tmA, tmB, s, e, lc)
-                          : launch_ffma_t<4, false>(cfg, tmA, tmB, s, e, lc);
+        G13_FFMA_CASE(2)
+        G13_FFMA_CASE(3)
+        G13_FFMA_CASE(4)
         default: return cudaErrorInvalidValue;
     }
+#undef G13_FFMA_CASE
 }
 
 }  // namespace g13

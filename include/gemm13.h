@@ -112,6 +112,8 @@ typedef struct {
     int32_t stage_a;      /* 1: A is first copied to an aligned plan workspace */
     int32_t stage_b;      /* 1: B likewise */
     int32_t num_ctas;     /* persistent grid size; 0 = one per SM */
+    int32_t variant;      /* family-specific main-loop variant; FFMA: 0 scalar FFMA,
+                             1 packed fma.rn.f32x2 (KN layout only) */
 } gemm_config_t;
 
 typedef struct gemm_plan_s* gemm_plan_t;

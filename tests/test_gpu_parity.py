@@ -79,11 +79,12 @@ def test_tc_variants_exact(cfg, dtype, layout):
     assert np.array_equal(C2, cref.reshape(C.shape)), f"{w.name} {cfg2} (2 CTAs)"
 
 
+@pytest.mark.parametrize("variant", [0, 1])
 @pytest.mark.parametrize("stages", [2, 3, 4])
 @pytest.mark.parametrize("layout", ["kn", "nk"])
-def test_ffma_variants_exact(stages, layout):
+def test_ffma_variants_exact(variant, stages, layout):
     w = _int_workload("f32", layout, 300, 260, 200)
-    run = Run(w, config=g13.Config("ffma", 128, 128, 32, stages))
+    run = Run(w, config=g13.Config("ffma", 128, 128, 32, stages, variant=variant))
     C = run.run().result()
     _, cref, _ = run.oracle()
     assert np.array_equal(C, cref.reshape(C.shape))

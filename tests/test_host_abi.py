@@ -106,7 +106,9 @@ def sel(dtype, M, N, K, layout="kn", sms=152, **kw):
 
 
 def test_dispatch_buckets(lib):
-    assert sel("f32", 4096, 4096, 4096).kernel == "ffma"
+    c = sel("f32", 4096, 4096, 4096)
+    assert (c.kernel, c.variant) == ("ffma", 1)        # packed FFMA2 main loop
+    assert sel("f32", 4096, 4096, 4096, "nk").variant == 0
     assert sel("f32", 256, 256, 256).kernel == "ffma"
     c = sel("bf16", 8192, 8192, 8192, "nk")
     assert (c.kernel, c.bm, c.bn, c.bk) == ("tc", 128, 256, 64)
