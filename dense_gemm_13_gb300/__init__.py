@@ -56,7 +56,7 @@ class _Config(ctypes.Structure):
                 ("bk", ctypes.c_int32), ("stages", ctypes.c_int32), ("split_k", ctypes.c_int32),
                 ("raster_group", ctypes.c_int32), ("stage_a", ctypes.c_int32),
                 ("stage_b", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
-                ("variant", ctypes.c_int32)]
+                ("variant", ctypes.c_int32), ("stream_k", ctypes.c_int32)]
 
 
 class _PlanInfo(ctypes.Structure):
@@ -168,10 +168,10 @@ class Config:
     """Python mirror of gemm_config_t."""
 
     def __init__(self, kernel="auto", bm=0, bn=0, bk=0, stages=0, split_k=1, raster_group=0,
-                 stage_a=0, stage_b=0, num_ctas=0, variant=0):
+                 stage_a=0, stage_b=0, num_ctas=0, variant=0, stream_k=0):
         self.kernel, self.bm, self.bn, self.bk, self.stages = kernel, bm, bn, bk, stages
         self.split_k, self.raster_group, self.stage_a, self.stage_b = split_k, raster_group, stage_a, stage_b
-        self.num_ctas, self.variant = num_ctas, variant
+        self.num_ctas, self.variant, self.stream_k = num_ctas, variant, stream_k
 
     def _c(self) -> _Config:
         c = _Config()
@@ -179,18 +179,20 @@ class Config:
         c.bm, c.bn, c.bk, c.stages = self.bm, self.bn, self.bk, self.stages
         c.split_k, c.raster_group = self.split_k, self.raster_group
         c.stage_a, c.stage_b, c.num_ctas = self.stage_a, self.stage_b, self.num_ctas
-        c.variant = self.variant
+        c.variant, c.stream_k = self.variant, self.stream_k
         return c
 
     @staticmethod
     def _from(c: _Config) -> "Config":
         return Config(KERNEL_NAMES.get(c.kernel, str(c.kernel)), c.bm, c.bn, c.bk, c.stages,
-                      c.split_k, c.raster_group, c.stage_a, c.stage_b, c.num_ctas, c.variant)
+                      c.split_k, c.raster_group, c.stage_a, c.stage_b, c.num_ctas, c.variant,
+                      c.stream_k)
 
     def as_dict(self) -> dict:
         return dict(kernel=self.kernel, bm=self.bm, bn=self.bn, bk=self.bk, stages=self.stages,
                     split_k=self.split_k, raster_group=self.raster_group, stage_a=self.stage_a,
-                    stage_b=self.stage_b, num_ctas=self.num_ctas, variant=self.variant)
+                    stage_b=self.stage_b, num_ctas=self.num_ctas, variant=self.variant,
+                    stream_k=self.stream_k)
 
     def __repr__(self):
         return f"Config({self.as_dict()})"

@@ -10,6 +10,7 @@
 
 #include <cstdio>
 #include <cstdlib>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -66,6 +67,9 @@ struct gemm_plan_s {
     size_t ws_b_off = 0;
     int64_t lda_s = 0, ldb_s = 0;        // leading dims of the staged copies
     int64_t stride_as = 0, stride_bs = 0;
+    size_t sk_off = 0, sk_tags_off = 0;   // stream-K partial slots and tags in d_ws
+    int64_t sk_grid = 0;
+    std::atomic<unsigned> epoch{0};       // tag counter for stream-K launches
     std::mutex mu;                        // guards the descriptor cache
     const void* mapA_src = nullptr;
     const void* mapB_src = nullptr;
@@ -159,6 +163,9 @@ int make_plan(const Problem& p, const gemm_config_t* forced, gemm_plan_t* out_pl
     if (rc != GEMM_OK) return rc;
     if (cfg.kernel == GEMM_KERNEL_TC && tc_smem_bytes(cfg) == 0) return GEMM_ERR_UNSUPPORTED;
     if (cfg.kernel == GEMM_KERNEL_FFMA && ffma_smem_bytes(cfg) == 0) return GEMM_ERR_UNSUPPORTED;
+    if (cfg.kernel == GEMM_KERNEL_FFMA &&
+        !ffma_units_ok(Shape{p.M, p.N, p.K, p.epi.batch, 1, 1}, cfg.bn))
+        return GEMM_ERR_UNSUPPORTED;
 
     gemm_plan_s* pl = new (std::nothrow) gemm_plan_s();
     if (!pl) return GEMM_ERR_OUT_OF_MEMORY;
@@ -185,9 +192,28 @@ int make_plan(const Problem& p, const gemm_config_t* forced, gemm_plan_t* out_pl
         pl->stride_bs = g.rows * pl->ldb_s;
         ws += static_cast<size_t>(round_up(g.batches * pl->stride_bs * esz, 256));
     }
+    if (cfg.kernel == GEMM_KERNEL_FFMA && cfg.stream_k) {
+        // Persistent grid: every CTA the device can hold at once (the launch is
+        // cooperative), and one 64 KB partial-sum slot plus a tag per CTA.
+        const int per_sm = ffma_ctas_per_sm(cfg, p.epi.b_layout);
+        if (per_sm <= 0) {
+            delete pl;
+            return GEMM_ERR_CUDA;
+        }
+        int64_t grid = static_cast<int64_t>(per_sm) * sms;
+        if (cfg.num_ctas > 0 && cfg.num_ctas < grid) grid = cfg.num_ctas;
+        pl->sk_grid = grid;
+        pl->sk_off = ws;
+        ws += static_cast<size_t>(grid) * ffma_partial_slot_bytes(cfg);
+        pl->sk_tags_off = ws;
+        ws += static_cast<size_t>(round_up(grid * 4, 256));
+    }
     ce = cudaMalloc(reinterpret_cast<void**>(&pl->d_status), sizeof(unsigned));
     if (ce == cudaSuccess) ce = cudaMemset(pl->d_status, 0, sizeof(unsigned));
     if (ce == cudaSuccess && ws > 0) ce = cudaMalloc(&pl->d_ws, ws);
+    if (ce == cudaSuccess && pl->sk_grid > 0)
+        ce = cudaMemset(static_cast<char*>(pl->d_ws) + pl->sk_tags_off, 0,
+                        static_cast<size_t>(pl->sk_grid) * 4);
     if (ce != cudaSuccess) {
         if (pl->d_status) cudaFree(pl->d_status);
         delete pl;
@@ -289,6 +315,14 @@ int gemm_run(gemm_plan_t plan, const void* A, const void* B, void* C, const void
     lc.flags = ep.flags;
     lc.num_sms = plan->num_sms;
     lc.stream = st;
+    if (plan->sk_grid > 0) {
+        lc.sk_partials = reinterpret_cast<float*>(static_cast<char*>(plan->d_ws) + plan->sk_off);
+        lc.sk_tags = reinterpret_cast<unsigned*>(static_cast<char*>(plan->d_ws) + plan->sk_tags_off);
+        lc.sk_grid = plan->sk_grid;
+        unsigned ep_tag = plan->epoch.fetch_add(1) + 1;
+        if (ep_tag == 0) ep_tag = plan->epoch.fetch_add(1) + 1;  // 0 marks "never written"
+        lc.sk_epoch = ep_tag;
+    }
 
     Shape s{p.M, p.N, p.K, ep.batch, 1, 1};
     const gemm_config_t& cfg = plan->cfg;
@@ -354,7 +388,8 @@ int gemm_run(gemm_plan_t plan, const void* A, const void* B, void* C, const void
                             128, CU_TENSOR_MAP_SWIZZLE_128B);
                 if (rc == GEMM_OK)
                     rc = kn ? encode(&plan->mapB, p.dtype, b_src, gb.cols, gb.rows, ldb, gb.batches,
-                                     sb, 128, 32, CU_TENSOR_MAP_SWIZZLE_NONE)
+                                     sb, static_cast<uint32_t>(cfg.bn), 32,
+                                     CU_TENSOR_MAP_SWIZZLE_NONE)
                             : encode(&plan->mapB, p.dtype, b_src, gb.cols, gb.rows, ldb, gb.batches,
                                      sb, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B);
             }

@@ -113,12 +113,24 @@ int choose_config(const Problem& p, int num_sms, gemm_config_t* out) {
     if (p.dtype == GEMM_F32) {
         c.kernel = GEMM_KERNEL_FFMA;
         c.bm = 128;
-        c.bn = 128;
         c.bk = 32;
-        c.stages = 3;
-        c.raster_group = 8;
+        const bool kn = p.epi.b_layout == GEMM_B_KN;
         // packed fma.rn.f32x2 main loop (KN layout): +17 % over scalar FFMA at 4096^3
-        c.variant = p.epi.b_layout == GEMM_B_KN ? 1 : 0;
+        c.variant = kn ? 1 : 0;
+        // Large KN problems: 128 x 256 tiles (8 x 16 per thread, one CTA per SM),
+        // which need a quarter less shared-memory bandwidth per FMA than 128 x 128
+        // (two CTAs per SM); 55.4 vs 51.7 TFLOPS at 4096^3 on GB300.
+        const bool wide = kn && bt * M * N >= (int64_t(1) << 22);
+        c.bn = wide ? 256 : 128;
+        c.stages = wide ? 4 : 3;
+        c.raster_group = wide ? 4 : 8;
+        // When whole-tile waves would leave more than a tenth of the CTA slots
+        // idle (4096^2 with 128 x 256 tiles: 512 tiles on 152 slots = 3.37
+        // waves), split (tile, K-step) units evenly over a persistent grid.
+        const int64_t slots = (wide ? 1 : 2) * static_cast<int64_t>(num_sms);
+        const int64_t tiles = bt * cdiv(M, 128) * cdiv(N, c.bn);
+        const int64_t waves = cdiv(tiles, slots);
+        c.stream_k = (tiles * 10 < waves * slots * 9) ? 1 : 0;
     } else {
         c.kernel = GEMM_KERNEL_TC;
         c.bm = 128;
@@ -152,17 +164,21 @@ int check_config(const Problem& p, const gemm_config_t& in, gemm_config_t* out) 
     switch (c.kernel) {
         case GEMM_KERNEL_SKINNY:
             c.stage_a = c.stage_b = 0;
+            if (c.stream_k != 0) return GEMM_ERR_UNSUPPORTED;
             break;
         case GEMM_KERNEL_FFMA:
             if (p.dtype != GEMM_F32 || p.K == 0) return GEMM_ERR_UNSUPPORTED;
             if (c.variant < 0 || c.variant > 1) return GEMM_ERR_UNSUPPORTED;
-            if (c.bm != 128 || c.bn != 128 || c.bk != 32) return GEMM_ERR_UNSUPPORTED;
+            if (c.stream_k < 0 || c.stream_k > 1) return GEMM_ERR_UNSUPPORTED;
+            if (c.bm != 128 || c.bk != 32) return GEMM_ERR_UNSUPPORTED;
+            if (c.bn != 128 && !(c.bn == 256 && p.epi.b_layout == GEMM_B_KN))
+                return GEMM_ERR_UNSUPPORTED;
             if (c.stages < 2 || c.stages > 4) return GEMM_ERR_UNSUPPORTED;
             if (c.raster_group == 0) c.raster_group = 8;
             break;
         case GEMM_KERNEL_TC:
             if (p.dtype == GEMM_F32 || p.K == 0) return GEMM_ERR_UNSUPPORTED;
-            if (c.variant != 0) return GEMM_ERR_UNSUPPORTED;
+            if (c.variant != 0 || c.stream_k != 0) return GEMM_ERR_UNSUPPORTED;
             if (c.bm != 128 || c.bk != 64) return GEMM_ERR_UNSUPPORTED;
             if (!((c.bn == 256 && (c.stages == 4 || c.stages == 3)) ||
                   (c.bn == 128 && (c.stages == 6 || c.stages == 4))))

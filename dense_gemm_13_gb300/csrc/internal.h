@@ -35,6 +35,11 @@ struct LaunchCtx {
     uint32_t flags;       // GEMM_FLAG_*
     int num_sms;
     cudaStream_t stream;
+    // stream-K (FFMA): partial-sum slots, their tags, grid size, this launch's tag
+    float* sk_partials;
+    unsigned* sk_tags;
+    int64_t sk_grid;
+    unsigned sk_epoch;
 };
 
 // Tensor-core path: A [batch][M][K] 16-bit via tmA (K innermost); B via tmB:
@@ -50,6 +55,12 @@ cudaError_t launch_ffma(const gemm_config_t& cfg, int b_layout, const CUtensorMa
                         const CUtensorMap& tmB, const Shape& s, const EpiParams& e,
                         const LaunchCtx& lc);
 size_t ffma_smem_bytes(const gemm_config_t& cfg);
+// Bytes of one stream-K partial-sum slot (one 128 x BN FP32 tile).
+size_t ffma_partial_slot_bytes(const gemm_config_t& cfg);
+// Whether the FFMA kernel can index this problem's (tile, K-step) units in 32 bits.
+bool ffma_units_ok(const Shape& s, int bn);
+// Resident CTAs per SM of the FFMA kernel a config selects (0 on error).
+int ffma_ctas_per_sm(const gemm_config_t& cfg, int b_layout);
 
 // Memory-bound path for small M or N: plain (unaligned-capable) loads.
 struct SkinnyArgs {

@@ -147,6 +147,7 @@ extern "C" int gemm_run_noalloc(gemm_dtype_t dtype, int64_t M, int64_t N, int64_
     gemm_config_t cfg;
     rc = choose_config(p, sms, &cfg);  // no cache: nothing is allocated, not even on the host
     if (rc != GEMM_OK) return rc;
+    cfg.stream_k = 0;  // whole tiles per CTA: stream-K partial slots would need more scratch
     const int esz = dtype_size(p.dtype);
     // Misaligned base pointers are staged too (the scratch is always there).
     if (cfg.kernel != GEMM_KERNEL_SKINNY) {
@@ -253,8 +254,8 @@ extern "C" int gemm_run_noalloc(gemm_dtype_t dtype, int64_t M, int64_t N, int64_
     rc = noalloc_encode(&mA, p.dtype, a_src, a_cols, a_rows, la, a_bat, sa, 32, 128,
                         CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc == GEMM_OK)
-        rc = kn ? noalloc_encode(&mB, p.dtype, b_src, b_cols, b_rows, lb, b_bat, sb, 128, 32,
-                                 CU_TENSOR_MAP_SWIZZLE_NONE)
+        rc = kn ? noalloc_encode(&mB, p.dtype, b_src, b_cols, b_rows, lb, b_bat, sb,
+                                 static_cast<uint32_t>(cfg.bn), 32, CU_TENSOR_MAP_SWIZZLE_NONE)
                 : noalloc_encode(&mB, p.dtype, b_src, b_cols, b_rows, lb, b_bat, sb, 32, 128,
                                  CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc != GEMM_OK) return rc;

@@ -114,6 +114,9 @@ typedef struct {
     int32_t num_ctas;     /* persistent grid size; 0 = one per SM */
     int32_t variant;      /* family-specific main-loop variant; FFMA: 0 scalar FFMA,
                              1 packed fma.rn.f32x2 (KN layout only) */
+    int32_t stream_k;     /* FFMA: 1 = persistent grid with (tile, K-step) units split evenly
+                             over the CTAs; tiles cut between CTAs are summed in a fixed order
+                             (deterministic).  Needs a plan workspace of grid x 64 KB. */
 } gemm_config_t;
 
 typedef struct gemm_plan_s* gemm_plan_t;

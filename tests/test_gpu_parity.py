@@ -79,16 +79,45 @@ def test_tc_variants_exact(cfg, dtype, layout):
     assert np.array_equal(C2, cref.reshape(C.shape)), f"{w.name} {cfg2} (2 CTAs)"
 
 
+@pytest.mark.parametrize("bn", [128, 256])
 @pytest.mark.parametrize("variant", [0, 1])
 @pytest.mark.parametrize("stages", [2, 3, 4])
 @pytest.mark.parametrize("layout", ["kn", "nk"])
-def test_ffma_variants_exact(variant, stages, layout):
-    w = _int_workload("f32", layout, 300, 260, 200)
-    run = Run(w, config=g13.Config("ffma", 128, 128, 32, stages, variant=variant))
+def test_ffma_variants_exact(bn, variant, stages, layout):
+    if bn == 256 and layout == "nk":
+        pytest.skip("256-wide FFMA tiles take row-major (KN) B only")
+    w = _int_workload("f32", layout, 300, 520, 200)
+    run = Run(w, config=g13.Config("ffma", 128, bn, 32, stages, variant=variant))
     C = run.run().result()
     _, cref, _ = run.oracle()
     assert np.array_equal(C, cref.reshape(C.shape))
     assert run.guard_ok()
+
+
+@pytest.mark.parametrize("num_ctas", [0, 1, 3, 7, 50])
+@pytest.mark.parametrize("bn,variant,layout", [(128, 1, "kn"), (128, 0, "kn"), (128, 0, "nk"),
+                                               (256, 1, "kn"), (256, 0, "kn")])
+def test_ffma_stream_k_exact(num_ctas, bn, variant, layout):
+    # 3 x 3 (or 3 x 2) tiles x 7 K steps spread over a persistent grid; with
+    # few CTAs a tile is cut between up to 8 of them and reassembled in order.
+    w = _int_workload("f32", layout, 300, 260, 200)
+    cfg = g13.Config("ffma", 128, bn, 32, 3, variant=variant, stream_k=1, num_ctas=num_ctas)
+    run = Run(w, config=cfg)
+    assert run.info["config"].stream_k == 1 and run.info["workspace_bytes"] > 0
+    C = run.run().result()
+    _, cref, _ = run.oracle()
+    assert np.array_equal(C, cref.reshape(C.shape)), f"{cfg}"
+    assert run.guard_ok()
+    # bit-identical on a second run (the partial-sum order is fixed)
+    C2 = run.run().result()
+    assert np.array_equal(C, C2)
+
+
+def test_ffma_stream_k_random_batched():
+    w = Workload("sk_batched", "f32", 200, 136, 650, batch=3, bias=True, act="relu",
+                 residual=True, beta=0.5)
+    run = Run(w, config=g13.Config("ffma", 128, 128, 32, 3, variant=1, stream_k=1, num_ctas=5))
+    full_check(run)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])

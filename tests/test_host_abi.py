@@ -107,7 +107,11 @@ def sel(dtype, M, N, K, layout="kn", sms=152, **kw):
 
 def test_dispatch_buckets(lib):
     c = sel("f32", 4096, 4096, 4096)
-    assert (c.kernel, c.variant) == ("ffma", 1)        # packed FFMA2 main loop
+    assert (c.kernel, c.variant, c.bn, c.stream_k) == ("ffma", 1, 256, 1)   # packed, wide, stream-K
+    c = sel("f32", 8192, 8192, 8192)
+    assert (c.bn, c.stream_k) == (256, 0)               # 2048 tiles = 13.5 waves: whole tiles
+    c = sel("f32", 256, 256, 256)
+    assert (c.bn, c.stream_k) == (128, 1)
     assert sel("f32", 4096, 4096, 4096, "nk").variant == 0
     assert sel("f32", 256, 256, 256).kernel == "ffma"
     c = sel("bf16", 8192, 8192, 8192, "nk")
