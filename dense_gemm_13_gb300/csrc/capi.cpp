@@ -74,6 +74,10 @@ struct gemm_plan_s {
     const void* mapA_src = nullptr;
     const void* mapB_src = nullptr;
     CUtensorMap mapA{}, mapB{};
+    const void* mapC_dst = nullptr;       // tensor-core epilogue descriptors (C, residual)
+    const void* mapR_src = nullptr;
+    bool epi_valid = false;
+    TcEpiMaps epi{};
 };
 
 namespace {
@@ -403,10 +407,51 @@ int gemm_run(gemm_plan_t plan, const void* A, const void* B, void* C, const void
         mA = plan->mapA;
         mB = plan->mapB;
     }
-    if (cfg.kernel == GEMM_KERNEL_TC)
-        ce = launch_tc(cfg, p.dtype, ep.b_layout, mA, mB, s, e, lc);
-    else
+    if (cfg.kernel != GEMM_KERNEL_TC) {
         ce = launch_ffma(cfg, ep.b_layout, mA, mB, s, e, lc);
+        return map_cuda_error(ce);
+    }
+    // Tensor-core epilogue through TMA when C (and an FP32 residual) allow it:
+    // 16-byte-aligned base, row stride and batch stride.
+    TcEpiMaps em;
+    bool use_em = false;
+    {
+        const uintptr_t cp = reinterpret_cast<uintptr_t>(C);
+        // TMA stores write whole 16-byte pieces of a row, so the descriptor
+        // covers the 16-byte-aligned prefix of each row; the kernel writes
+        // the remaining < 16 bytes itself.
+        const int64_t n_tma = p.N / (16 / osz) * (16 / osz);
+        const bool c_ok = cp % 16 == 0 && (p.ldc * osz) % 16 == 0 && n_tma > 0 &&
+                          (ep.batch == 1 || (ep.stride_c * osz) % 16 == 0);
+        if (c_ok) {
+            std::lock_guard<std::mutex> lk(plan->mu);
+            if (!plan->epi_valid || plan->mapC_dst != C || plan->mapR_src != residual) {
+                TcEpiMaps m{};
+                int rc = encode(&m.c, ep.out_dtype, C, n_tma, p.M, p.ldc, ep.batch,
+                                ep.stride_c, osz == 4 ? 32u : 64u, 32u, CU_TENSOR_MAP_SWIZZLE_128B);
+                m.n_tma = n_tma;
+                const uintptr_t rp = reinterpret_cast<uintptr_t>(residual);
+                const bool r_shared = ep.batch > 1 && ep.stride_r == 0;
+                m.r_tma = residual && osz == 4 && rp % 16 == 0 && (ep.ldr * 4) % 16 == 0 &&
+                          (ep.batch == 1 || r_shared || (ep.stride_r * 4) % 16 == 0);
+                if (rc == GEMM_OK && m.r_tma)
+                    rc = encode(&m.r, GEMM_F32, residual, p.N, p.M, ep.ldr,
+                                r_shared ? 1 : ep.batch, ep.stride_r, 32u, 32u,
+                                CU_TENSOR_MAP_SWIZZLE_128B);
+                m.c_bmul = ep.batch > 1 ? 1 : 0;
+                m.r_bmul = (ep.batch > 1 && !r_shared) ? 1 : 0;
+                plan->epi_valid = rc == GEMM_OK;
+                plan->epi = m;
+                plan->mapC_dst = C;
+                plan->mapR_src = residual;
+            }
+            if (plan->epi_valid) {
+                em = plan->epi;
+                use_em = true;
+            }
+        }
+    }
+    ce = launch_tc(cfg, p.dtype, ep.b_layout, mA, mB, use_em ? &em : nullptr, s, e, lc);
     return map_cuda_error(ce);
 }
 

@@ -42,11 +42,21 @@ struct LaunchCtx {
     unsigned sk_epoch;
 };
 
+// TMA descriptors for the tensor-core epilogue: C (box of 32 rows x 128 bytes,
+// 128B swizzle) and, when r_tma, the FP32 residual (32 x 32, 128B swizzle).
+struct TcEpiMaps {
+    CUtensorMap c, r;
+    int r_tma;
+    int c_bmul, r_bmul;  // batch coordinate multipliers (0: shared across the batch)
+    int64_t n_tma;       // columns covered by the C descriptor (N rounded down to 16 bytes)
+};
+
 // Tensor-core path: A [batch][M][K] 16-bit via tmA (K innermost); B via tmB:
-// NK layout -> dims (K, N, batch), KN layout -> dims (N, K, batch).
+// NK layout -> dims (K, N, batch), KN layout -> dims (N, K, batch).  With em
+// null the epilogue stores C from registers.
 cudaError_t launch_tc(const gemm_config_t& cfg, int dtype, int b_layout, const CUtensorMap& tmA,
-                      const CUtensorMap& tmB, const Shape& s, const EpiParams& e,
-                      const LaunchCtx& lc);
+                      const CUtensorMap& tmB, const TcEpiMaps* em, const Shape& s,
+                      const EpiParams& e, const LaunchCtx& lc);
 // Shared memory the TC kernel needs for a config (bytes), or 0 if unsupported.
 size_t tc_smem_bytes(const gemm_config_t& cfg);
 

@@ -249,7 +249,7 @@ extern "C" int gemm_run_noalloc(gemm_dtype_t dtype, int64_t M, int64_t N, int64_
                                 kn ? 64u : static_cast<uint32_t>(cfg.bn),
                                 CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc != GEMM_OK) return rc;
-        return status_of(launch_tc(cfg, p.dtype, ep.b_layout, mA, mB, s, e, lc));
+        return status_of(launch_tc(cfg, p.dtype, ep.b_layout, mA, mB, nullptr, s, e, lc));
     }
     rc = noalloc_encode(&mA, p.dtype, a_src, a_cols, a_rows, la, a_bat, sa, 32, 128,
                         CU_TENSOR_MAP_SWIZZLE_128B);

@@ -14,7 +14,13 @@
 //               hands finished accumulators to the epilogue (tfull[buf]).
 //   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns at a time, apply
 //               alpha / bias / activation / residual / cast, store C once,
-//               release the accumulator buffer (tempty[buf]).
+//               release the accumulator buffer (tempty[buf]).  Each warp
+//               works on 128-byte-wide column chunks of its 32 rows: the
+//               values go into a double-buffered 128B-swizzled shared tile
+//               that one lane writes out with a TMA store (coalesced,
+//               asynchronous, clipped at the matrix edge); an FP32 residual
+//               arrives the same way, by a TMA load into that tile first.
+//               Layouts TMA cannot address fall back to per-thread stores.
 //
 // The grid is persistent (one CTA per SM); CTA c walks tiles c, c+grid, ...
 // in a grouped raster order.  The double-buffered accumulator lets the
@@ -36,6 +42,8 @@ namespace {
 
 constexpr int TBM = 128, TBK = 64, TTHREADS = 192;
 constexpr int T_A_BYTES = TBM * TBK * 2;  // 16 KB: 128 rows x 128 B
+constexpr int EPI_WARPS = 4;
+constexpr int EPI_BUF_BYTES = 32 * 128;   // one 32-row x 128-byte output (or residual) chunk
 
 template <int BN>
 struct TcLayout {
@@ -46,6 +54,13 @@ struct TcLayout {
 struct TcArgs {
     int64_t M, N, K, batch;
     int a_bmul, b_bmul;
+    int epi_tma;    // 1: C is written by TMA stores through shared memory
+    int r_tma;      // 1: the FP32 residual is read by TMA loads (implies epi_tma)
+    int out16;      // 1: C holds 16-bit values (64 columns per 128-byte chunk)
+    int c_bmul, r_bmul;
+    int bias_vec;   // 1: bias is 16-byte aligned (float4 loads)
+    int64_t n_tma;  // columns [0, n_tma) go out by TMA (a multiple of 16 bytes); the rest,
+                    // fewer than 16 bytes per row, from registers
     int64_t m_tiles, n_tiles, tiles_per_batch, total_tiles;
     int k_blocks;
     int raster;
@@ -57,13 +72,18 @@ struct TcArgs {
 };
 
 template <int BN, int STAGES>
-__host__ __device__ constexpr int tc_bar_off() {
+__host__ __device__ constexpr int tc_epi_off() {
     return STAGES * TcLayout<BN>::STAGE_BYTES;
 }
 template <int BN, int STAGES>
+__host__ __device__ constexpr int tc_bar_off() {
+    return tc_epi_off<BN, STAGES>() + EPI_WARPS * 2 * EPI_BUF_BYTES;
+}
+template <int BN, int STAGES>
 __host__ __device__ constexpr int tc_smem_total() {
-    // ring + full/empty per stage + tfull/tempty x2 + drain + tmem slot + abort flag
-    return 1024 + tc_bar_off<BN, STAGES>() + (2 * STAGES + 5) * 8 + 16;
+    // ring + epilogue tiles + full/empty per stage + tfull/tempty x2 + drain
+    // + residual barriers (2 per epilogue warp) + tmem slot + abort flag
+    return 1024 + tc_bar_off<BN, STAGES>() + (2 * STAGES + 5 + 2 * EPI_WARPS) * 8 + 16;
 }
 
 __device__ __forceinline__ void tc_tile_coords(int64_t t, const TcArgs& a, int64_t& b, int64_t& mt,
@@ -88,6 +108,7 @@ __device__ __forceinline__ void tc_drain(uint32_t bar, uint32_t parity, uint64_t
 template <int BN, int STAGES, bool B_KN>
 __global__ void __launch_bounds__(TTHREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmR,
                    const TcArgs args) {
     using L = TcLayout<BN>;
     constexpr uint32_t TMEM_COLS = 2 * BN;  // 256 or 512: powers of two
@@ -99,7 +120,8 @@ __global__ void __launch_bounds__(TTHREADS, 1)
     uint64_t* tfull = empty + STAGES;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* rbar = drain + 1;  // [EPI_WARPS][2] residual-chunk barriers
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rbar + 2 * EPI_WARPS);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -114,6 +136,7 @@ __global__ void __launch_bounds__(TTHREADS, 1)
             mbar_init(smem_u32(&tempty[i]), 128);
         }
         mbar_init(smem_u32(drain), 1);
+        for (int i = 0; i < 2 * EPI_WARPS; ++i) mbar_init(smem_u32(&rbar[i]), 1);
         *abort_flag = 0u;
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
@@ -240,38 +263,196 @@ __global__ void __launch_bounds__(TTHREADS, 1)
         }
     } else {
         // ---------------------------------------------------- epilogue warps
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int ew = warp - 2;  // 0 .. EPI_WARPS-1
+        const int q = warp & 3;   // TMEM lane quarter this warp may access
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+        uint8_t* etile = smem + tc_epi_off<BN, STAGES>() + ew * 2 * EPI_BUF_BYTES;
+        uint64_t* rb = rbar + 2 * ew;
+        const EpiParams& e = args.e;
+        uint32_t rph = 0;  // bit i: phase parity of rb[i]
+        int nchunk = 0;    // chunks this warp has staged (selects the buffer)
+        bool ok = true;
         int lt = 0;
-        for (int64_t t = blockIdx.x; t < args.total_tiles; t += gridDim.x, ++lt) {
+        for (int64_t t = blockIdx.x; ok && t < args.total_tiles; t += gridDim.x, ++lt) {
             const int buf = lt & 1;
             const uint32_t tph = static_cast<uint32_t>(lt >> 1) & 1u;
             if (!mbar_wait_bounded(smem_u32(&tfull[buf]), tph, abort_flag, args.status, tmo)) break;
             tc_fence_after();
             int64_t b, mt, nt;
             tc_tile_coords(t, args, b, mt, nt);
-            const int64_t row = mt * TBM + q * 32 + lane;
+            const int32_t row0 = static_cast<int32_t>(mt * TBM + q * 32);
+            const int64_t row = row0 + lane;
             const int64_t col0 = nt * BN;
+            const uint32_t tbase = tmem_base + lane_base + static_cast<uint32_t>(buf * BN);
+            if (args.epi_tma) {
+                const int W = args.out16 ? 64 : 32;  // columns per 128-byte chunk
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tmem_base + lane_base + static_cast<uint32_t>(buf * BN + c * 32),
-                                   r);
-                tmem_ld_wait();
-                if (c == BN / 32 - 1) {
-                    // All of this buffer is in registers: hand it back to the MMA warp.
-                    tc_fence_before();
-                    mbar_arrive(smem_u32(&tempty[buf]));
-                }
-                if (col0 + c * 32 < args.e.N) {
+                for (int c = 0; c < BN; c += W) {
+                    uint32_t v[64];
+                    tmem_ld_32x32b_x32(tbase + c, *reinterpret_cast<uint32_t(*)[32]>(v));
+                    if (W == 64)
+                        tmem_ld_32x32b_x32(tbase + c + 32,
+                                           *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+                    tmem_ld_wait();
+                    if (c + W >= BN) {
+                        // All of this accumulator is in registers: hand it back.
+                        tc_fence_before();
+                        mbar_arrive(smem_u32(&tempty[buf]));
+                    }
+                    const int64_t cg = col0 + c;  // first global column of the chunk
+                    if (cg >= e.N) continue;
+                    const int sel = nchunk & 1;
+                    ++nchunk;
+                    uint8_t* sb = etile + sel * EPI_BUF_BYTES;
+                    // The TMA store issued from this buffer two chunks ago must
+                    // have finished reading it.
+                    if (lane == 0) bulk_wait_read<1>();
+                    __syncwarp();
+                    if (args.r_tma && lane == 0) {
+                        mbar_arrive_expect_tx(smem_u32(&rb[sel]), EPI_BUF_BYTES);
+                        tma_load_3d(smem_u32(sb), &tmR, smem_u32(&rb[sel]),
+                                    static_cast<int32_t>(cg), row0,
+                                    static_cast<int32_t>(b * args.r_bmul));
+                    }
+                    float y[64];
 #pragma unroll
-                    for (int g = 0; g < 8; ++g)
-                        epi_store4(args.e, b, row, col0 + c * 32 + 4 * g,
-                                   __uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
-                                   __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
+                    for (int i = 0; i < 64; ++i)
+                        if (i < W) y[i] = __uint_as_float(v[i]) * e.alpha;
+                    if (e.bias) {
+                        const float* bp = e.bias + cg;
+                        if (args.bias_vec && cg + W <= e.N) {
+#pragma unroll
+                            for (int i = 0; i < 64; i += 4)
+                                if (i < W) {
+                                    const float4 bv = __ldg(reinterpret_cast<const float4*>(bp + i));
+                                    y[i] += bv.x;
+                                    y[i + 1] += bv.y;
+                                    y[i + 2] += bv.z;
+                                    y[i + 3] += bv.w;
+                                }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 64; ++i)
+                                if (i < W && cg + i < e.N) y[i] += __ldg(bp + i);
+                        }
+                    }
+                    if (e.act == GEMM_ACT_GELU_ERF) {
+#pragma unroll
+                        for (int i = 0; i < 64; ++i)
+                            if (i < W) y[i] = epi_act(GEMM_ACT_GELU_ERF, y[i]);
+                    } else if (e.act == GEMM_ACT_RELU) {
+#pragma unroll
+                        for (int i = 0; i < 64; ++i)
+                            if (i < W) y[i] = fmaxf(y[i], 0.0f);
+                    }
+                    // 16-byte chunk j of this thread's row sits at position j ^ (row & 7).
+                    uint8_t* rowp = sb + lane * 128;
+                    if (e.R) {
+                        if (args.r_tma) {
+                            if (!mbar_wait_bounded(smem_u32(&rb[sel]), (rph >> sel) & 1u, abort_flag,
+                                                   args.status, tmo)) {
+                                tc_drain(smem_u32(&rb[sel]), (rph >> sel) & 1u, tmo);
+                                ok = false;
+                                break;
+                            }
+                            rph ^= 1u << sel;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const float4 r4 =
+                                    *reinterpret_cast<const float4*>(rowp + ((j ^ (lane & 7)) << 4));
+                                y[4 * j] += e.beta * r4.x;
+                                y[4 * j + 1] += e.beta * r4.y;
+                                y[4 * j + 2] += e.beta * r4.z;
+                                y[4 * j + 3] += e.beta * r4.w;
+                            }
+                        } else if (row < e.M) {
+                            const float* rp = e.R + b * e.stride_r + row * e.ldr + cg;
+#pragma unroll
+                            for (int i = 0; i < 64; ++i)
+                                if (i < W && cg + i < e.N) y[i] += e.beta * __ldg(rp + i);
+                        }
+                    }
+                    if (!args.out16) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            *reinterpret_cast<float4*>(rowp + ((j ^ (lane & 7)) << 4)) =
+                                make_float4(y[4 * j], y[4 * j + 1], y[4 * j + 2], y[4 * j + 3]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            uint32_t w4[4];
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                const float lo = y[8 * j + 2 * h], hi = y[8 * j + 2 * h + 1];
+                                if (e.out_dtype == GEMM_BF16) {
+                                    __nv_bfloat162 p2 = __floats2bfloat162_rn(lo, hi);
+                                    w4[h] = *reinterpret_cast<uint32_t*>(&p2);
+                                } else {
+                                    __half2 p2 = __floats2half2_rn(lo, hi);
+                                    w4[h] = *reinterpret_cast<uint32_t*>(&p2);
+                                }
+                            }
+                            *reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4)) =
+                                make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && cg < args.n_tma) {
+                        tma_store_3d(&tmC, smem_u32(sb), static_cast<int32_t>(cg), row0,
+                                     static_cast<int32_t>(b * args.c_bmul));
+                        bulk_commit();
+                    }
+                    if (cg + W > args.n_tma && row < e.M) {
+                        // Ragged right edge: TMA stores whole 16-byte pieces, so the
+                        // last < 16 bytes of each row (columns n_tma .. N-1, all in
+                        // one 16-byte piece of this chunk) are copied from the
+                        // shared tile by the row's own thread.
+                        const int jt = static_cast<int>((args.n_tma - cg) * (args.out16 ? 2 : 4) / 16);
+                        const uint4 piece =
+                            *reinterpret_cast<const uint4*>(rowp + ((jt ^ (lane & 7)) << 4));
+                        const int64_t base = b * e.stride_c + row * e.ldc + args.n_tma;
+                        const int nrest = static_cast<int>(e.N - args.n_tma);
+                        if (!args.out16) {
+                            const float f[4] = {__uint_as_float(piece.x), __uint_as_float(piece.y),
+                                                __uint_as_float(piece.z), __uint_as_float(piece.w)};
+#pragma unroll
+                            for (int t = 0; t < 3; ++t)
+                                if (t < nrest) static_cast<float*>(e.C)[base + t] = f[t];
+                        } else {
+                            const uint32_t w[4] = {piece.x, piece.y, piece.z, piece.w};
+#pragma unroll
+                            for (int t = 0; t < 7; ++t)
+                                if (t < nrest)
+                                    static_cast<uint16_t*>(e.C)[base + t] =
+                                        static_cast<uint16_t>(w[t >> 1] >> (16 * (t & 1)));
+                        }
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c * 32), r);
+                    tmem_ld_wait();
+                    if (c == BN / 32 - 1) {
+                        // All of this buffer is in registers: hand it back to the MMA warp.
+                        tc_fence_before();
+                        mbar_arrive(smem_u32(&tempty[buf]));
+                    }
+                    if (col0 + c * 32 < e.N) {
+#pragma unroll
+                        for (int g = 0; g < 8; ++g)
+                            epi_store4(e, b, row, col0 + c * 32 + 4 * g, __uint_as_float(r[4 * g]),
+                                       __uint_as_float(r[4 * g + 1]), __uint_as_float(r[4 * g + 2]),
+                                       __uint_as_float(r[4 * g + 3]));
+                    }
                 }
             }
         }
+        // Shared memory must outlive the TMA stores that read it.
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -285,8 +466,8 @@ __global__ void __launch_bounds__(TTHREADS, 1)
 
 template <int BN, int STAGES, bool B_KN>
 cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& tmA,
-                        const CUtensorMap& tmB, const Shape& s, const EpiParams& e,
-                        const LaunchCtx& lc) {
+                        const CUtensorMap& tmB, const TcEpiMaps* em, const Shape& s,
+                        const EpiParams& e, const LaunchCtx& lc) {
     TcArgs a{};
     a.M = s.M;
     a.N = s.N;
@@ -294,6 +475,14 @@ cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& 
     a.batch = s.batch;
     a.a_bmul = s.a_bmul;
     a.b_bmul = s.b_bmul;
+    static const CUtensorMap unused_map{};
+    a.epi_tma = em != nullptr;
+    a.r_tma = em != nullptr && em->r_tma;
+    a.out16 = e.out_dtype != GEMM_F32;
+    a.c_bmul = em ? em->c_bmul : 0;
+    a.r_bmul = em ? em->r_bmul : 0;
+    a.bias_vec = e.bias && (reinterpret_cast<uintptr_t>(e.bias) % 16 == 0);
+    a.n_tma = em ? em->n_tma : 0;
     a.m_tiles = (s.M + TBM - 1) / TBM;
     a.n_tiles = (s.N + BN - 1) / BN;
     a.tiles_per_batch = a.m_tiles * a.n_tiles;
@@ -317,22 +506,23 @@ cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& 
     int64_t grid = cfg.num_ctas > 0 ? cfg.num_ctas : lc.num_sms;
     if (grid > a.total_tiles) grid = a.total_tiles;
     if (grid < 1) grid = 1;
-    kern<<<static_cast<unsigned>(grid), TTHREADS, smem, lc.stream>>>(tmA, tmB, a);
+    kern<<<static_cast<unsigned>(grid), TTHREADS, smem, lc.stream>>>(
+        tmA, tmB, em ? em->c : unused_map, (em && em->r_tma) ? em->r : unused_map, a);
     return cudaGetLastError();
 }
 
 template <bool B_KN>
 cudaError_t launch_tc_layout(const gemm_config_t& cfg, int dtype, const CUtensorMap& tmA,
-                             const CUtensorMap& tmB, const Shape& s, const EpiParams& e,
-                             const LaunchCtx& lc) {
+                             const CUtensorMap& tmB, const TcEpiMaps* em, const Shape& s,
+                             const EpiParams& e, const LaunchCtx& lc) {
     if (cfg.bn == 256 && cfg.stages == 4)
-        return launch_tc_t<256, 4, B_KN>(cfg, dtype, tmA, tmB, s, e, lc);
+        return launch_tc_t<256, 4, B_KN>(cfg, dtype, tmA, tmB, em, s, e, lc);
     if (cfg.bn == 256 && cfg.stages == 3)
-        return launch_tc_t<256, 3, B_KN>(cfg, dtype, tmA, tmB, s, e, lc);
+        return launch_tc_t<256, 3, B_KN>(cfg, dtype, tmA, tmB, em, s, e, lc);
     if (cfg.bn == 128 && cfg.stages == 6)
-        return launch_tc_t<128, 6, B_KN>(cfg, dtype, tmA, tmB, s, e, lc);
+        return launch_tc_t<128, 6, B_KN>(cfg, dtype, tmA, tmB, em, s, e, lc);
     if (cfg.bn == 128 && cfg.stages == 4)
-        return launch_tc_t<128, 4, B_KN>(cfg, dtype, tmA, tmB, s, e, lc);
+        return launch_tc_t<128, 4, B_KN>(cfg, dtype, tmA, tmB, em, s, e, lc);
     return cudaErrorInvalidValue;
 }
 
@@ -348,10 +538,10 @@ size_t tc_smem_bytes(const gemm_config_t& cfg) {
 }
 
 cudaError_t launch_tc(const gemm_config_t& cfg, int dtype, int b_layout, const CUtensorMap& tmA,
-                      const CUtensorMap& tmB, const Shape& s, const EpiParams& e,
-                      const LaunchCtx& lc) {
-    if (b_layout == GEMM_B_KN) return launch_tc_layout<true>(cfg, dtype, tmA, tmB, s, e, lc);
-    return launch_tc_layout<false>(cfg, dtype, tmA, tmB, s, e, lc);
+                      const CUtensorMap& tmB, const TcEpiMaps* em, const Shape& s,
+                      const EpiParams& e, const LaunchCtx& lc) {
+    if (b_layout == GEMM_B_KN) return launch_tc_layout<true>(cfg, dtype, tmA, tmB, em, s, e, lc);
+    return launch_tc_layout<false>(cfg, dtype, tmA, tmB, em, s, e, lc);
 }
 
 }  // namespace g13

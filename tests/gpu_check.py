@@ -44,7 +44,7 @@ class Run:
 
     def __init__(self, w: Workload, tensors: dict | None = None, config: g13.Config | None = None,
                  seed: int = 0, guard: bool = True, a_offset: int = 0, b_offset: int = 0,
-                 plan: g13.Plan | None = None):
+                 plan: g13.Plan | None = None, ldc_pad: int = 0):
         self.w = w
         self.t = tensors if tensors is not None else w.make(seed)
         dev = torch.device("cuda")
@@ -56,12 +56,14 @@ class Run:
         self.dR = self.t["R"].to(dev) if self.t["R"] is not None else None
         bt, M, N = w.batch, w.M, w.N
         odt = TORCH_OUT[w.out_dtype]
-        # guard bands: one NaN row above and below, 4 NaN columns on the left and
-        # at least 12 on the right; C's start stays 16-byte (f32) / 8-byte aligned.
+        # guard bands: one NaN row above and below, 8 NaN columns on the left and
+        # at least 8 on the right; C's start and row stride stay 16-byte aligned
+        # (the TMA-store epilogue) unless ldc_pad makes the row stride odd (the
+        # per-thread fallback).
         self.g = 1 if guard else 0
-        self.ldc = (N + 7) // 8 * 8 + 16 if guard else max(N, 1)
+        self.ldc = ((N + 7) // 8 * 8 + 16 if guard else max(N, 1)) + ldc_pad
         self.cbuf = torch.full((bt, M + 2 * self.g, self.ldc), float("nan"), dtype=odt, device=dev)
-        self.C = self.cbuf[:, self.g:self.g + M, 4 * self.g:4 * self.g + N]
+        self.C = self.cbuf[:, self.g:self.g + M, 8 * self.g:8 * self.g + N]
         lda = A.shape[-1] if A.shape[-1] > 0 else 1
         ldb = B.shape[-1] if B.shape[-1] > 0 else 1
         ep = g13.Epilogue(b_layout=w.b_layout, out_dtype=w.out_dtype, bias=w.bias, act=w.act,
@@ -100,7 +102,7 @@ class Run:
         torch.cuda.synchronize()
         mask = torch.ones(self.cbuf.shape, dtype=torch.bool, device=self.cbuf.device)
         g = self.g
-        mask[:, g:g + self.w.M, 4 * g:4 * g + self.w.N] = False
+        mask[:, g:g + self.w.M, 8 * g:8 * g + self.w.N] = False
         return bool(torch.isnan(self.cbuf[mask].float()).all().item())
 
     # ------------------------------------------------------------ oracle

@@ -156,6 +156,38 @@ def test_epilogue_variants(epi, dtype):
     full_check(Run(w, seed=4))
 
 
+@pytest.mark.parametrize("epi", [dict(), dict(residual=True, bias=True, act="gelu", beta=-1.25),
+                                 dict(out_dtype="bf16", bias=True, act="gelu"),
+                                 dict(out_dtype="f16", residual=True)],
+                         ids=["plain", "res-bias-gelu", "bf16-gelu", "f16-res"])
+@pytest.mark.parametrize("ldc_pad", [1, 3])
+def test_epilogue_unaligned_c(epi, ldc_pad):
+    # odd row strides of C: the tensor-core epilogue cannot use TMA stores and
+    # writes from registers instead; results must be the same
+    for layout in ("kn", "nk"):
+        w = Workload(f"epi_odd_ldc_{layout}", "bf16", 333, 520, 200, b_layout=layout, alpha=0.75,
+                     **epi)
+        full_check(Run(w, seed=5, ldc_pad=ldc_pad))
+
+
+@pytest.mark.parametrize("batch_r", [True, False])
+def test_batched_residual_tma(batch_r):
+    # batched FP32 residual read by TMA (per-batch R, or one R shared by all entries)
+    bt, M, N, K = 4, 200, 264, 136
+    A = matrix((bt, M, K), "normal", 0, "bf16")
+    B = matrix((bt, K, N), "normal", 1, "bf16")
+    R = matrix((bt, M, N) if batch_r else (M, N), "normal", 3, "f32")
+    w = Workload("bres", "bf16", M, N, K, batch=bt, residual=True, beta=0.5)
+    run = Run(w, tensors={"A": A, "B": B, "bias": None, "R": R})
+    if not batch_r:
+        run.plan = g13.gemm_plan("bf16", M, N, K, K, N, run.ldc,
+                                 g13.Epilogue(residual=True, beta=0.5, ldr=N, batch=bt,
+                                              stride_a=M * K, stride_b=K * N,
+                                              stride_c=run.cbuf.shape[-1] * run.cbuf.shape[-2],
+                                              stride_r=0))
+    full_check(run)
+
+
 # ---------------------------------------------------------------- named workloads
 @pytest.mark.parametrize("name", ["sgemm_256", "qkt_bf16", "qkt_f16"])
 def test_workload_full(name):

@@ -57,7 +57,7 @@ def test_noalloc_matches_planned_path_twice_in_a_row():
     for w, a_off, b_off in CASES:
         run = Run(w, seed=11, a_offset=a_off, b_offset=b_off)
         C = torch.full(run.cbuf.shape, float("nan"), dtype=TORCH_OUT[w.out_dtype],
-                       device="cuda")[:, 1:1 + w.M, 4:4 + w.N]
+                       device="cuda")[:, 1:1 + w.M, 8:8 + w.N]
         rc = _noalloc_call(run, C, stream)
         assert rc == 0, g13.gemm_strerror(rc)
         runs.append(run)
