@@ -149,6 +149,13 @@ int choose_config(const Problem& p, int num_sms, gemm_config_t* out) {
             c.bn = 256;
             c.stages = 4;
         }
+        // Short K: the epilogue (per output) weighs as much as the main loop
+        // (per output, per K step), so give it eight warps -- two per TMEM lane
+        // quarter -- at the cost of one or two pipeline stages.
+        if (K <= 1024) {
+            c.variant = 1;
+            c.stages = c.bn == 256 ? 3 : 4;
+        }
         c.raster_group = static_cast<int32_t>(std::min<int64_t>(16, mt));
     }
     set_staging(p, &c);
@@ -178,10 +185,13 @@ int check_config(const Problem& p, const gemm_config_t& in, gemm_config_t* out) 
             break;
         case GEMM_KERNEL_TC:
             if (p.dtype == GEMM_F32 || p.K == 0) return GEMM_ERR_UNSUPPORTED;
-            if (c.variant != 0 || c.stream_k != 0) return GEMM_ERR_UNSUPPORTED;
+            if (c.stream_k != 0) return GEMM_ERR_UNSUPPORTED;
             if (c.bm != 128 || c.bk != 64) return GEMM_ERR_UNSUPPORTED;
-            if (!((c.bn == 256 && (c.stages == 4 || c.stages == 3)) ||
-                  (c.bn == 128 && (c.stages == 6 || c.stages == 4))))
+            // (BN, stages) pairs with 4 epilogue warps (variant 0) or 8 (variant 1)
+            if (!((c.variant == 0 && ((c.bn == 256 && (c.stages == 4 || c.stages == 3)) ||
+                                      (c.bn == 128 && (c.stages == 6 || c.stages == 4)))) ||
+                  (c.variant == 1 && ((c.bn == 256 && c.stages == 3) ||
+                                      (c.bn == 128 && c.stages == 4)))))
                 return GEMM_ERR_UNSUPPORTED;
             if (c.raster_group == 0) c.raster_group = 16;
             break;

@@ -40,9 +40,8 @@
 namespace g13 {
 namespace {
 
-constexpr int TBM = 128, TBK = 64, TTHREADS = 192;
+constexpr int TBM = 128, TBK = 64;
 constexpr int T_A_BYTES = TBM * TBK * 2;  // 16 KB: 128 rows x 128 B
-constexpr int EPI_WARPS = 4;
 constexpr int EPI_BUF_BYTES = 32 * 128;   // one 32-row x 128-byte output (or residual) chunk
 
 template <int BN>
@@ -71,19 +70,25 @@ struct TcArgs {
     uint32_t flags;
 };
 
+// EW epilogue warps: 4 (one per TMEM lane quarter) or 8 (two per quarter,
+// each taking half of the columns).
+template <int EW>
+__host__ __device__ constexpr int tc_threads() {
+    return 64 + 32 * EW;
+}
 template <int BN, int STAGES>
 __host__ __device__ constexpr int tc_epi_off() {
     return STAGES * TcLayout<BN>::STAGE_BYTES;
 }
-template <int BN, int STAGES>
+template <int BN, int STAGES, int EW>
 __host__ __device__ constexpr int tc_bar_off() {
-    return tc_epi_off<BN, STAGES>() + EPI_WARPS * 2 * EPI_BUF_BYTES;
+    return tc_epi_off<BN, STAGES>() + EW * 2 * EPI_BUF_BYTES;
 }
-template <int BN, int STAGES>
+template <int BN, int STAGES, int EW>
 __host__ __device__ constexpr int tc_smem_total() {
     // ring + epilogue tiles + full/empty per stage + tfull/tempty x2 + drain
     // + residual barriers (2 per epilogue warp) + tmem slot + abort flag
-    return 1024 + tc_bar_off<BN, STAGES>() + (2 * STAGES + 5 + 2 * EPI_WARPS) * 8 + 16;
+    return 1024 + tc_bar_off<BN, STAGES, EW>() + (2 * STAGES + 5 + 2 * EW) * 8 + 16;
 }
 
 __device__ __forceinline__ void tc_tile_coords(int64_t t, const TcArgs& a, int64_t& b, int64_t& mt,
@@ -105,8 +110,8 @@ __device__ __forceinline__ void tc_drain(uint32_t bar, uint32_t parity, uint64_t
         if (globaltimer_ns() - t0 > timeout_ns) return;
 }
 
-template <int BN, int STAGES, bool B_KN>
-__global__ void __launch_bounds__(TTHREADS, 1)
+template <int BN, int STAGES, bool B_KN, int EW>
+__global__ void __launch_bounds__(tc_threads<EW>(), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmR,
                    const TcArgs args) {
@@ -115,13 +120,13 @@ __global__ void __launch_bounds__(TTHREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + tc_bar_off<BN, STAGES>());
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + tc_bar_off<BN, STAGES, EW>());
     uint64_t* empty = full + STAGES;
     uint64_t* tfull = empty + STAGES;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
-    uint64_t* rbar = drain + 1;  // [EPI_WARPS][2] residual-chunk barriers
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rbar + 2 * EPI_WARPS);
+    uint64_t* rbar = drain + 1;  // [EW][2] residual-chunk barriers
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rbar + 2 * EW);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -133,10 +138,10 @@ __global__ void __launch_bounds__(TTHREADS, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&tfull[i]), 1);
-            mbar_init(smem_u32(&tempty[i]), 128);
+            mbar_init(smem_u32(&tempty[i]), 32 * EW);
         }
         mbar_init(smem_u32(drain), 1);
-        for (int i = 0; i < 2 * EPI_WARPS; ++i) mbar_init(smem_u32(&rbar[i]), 1);
+        for (int i = 0; i < 2 * EW; ++i) mbar_init(smem_u32(&rbar[i]), 1);
         *abort_flag = 0u;
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
@@ -263,8 +268,11 @@ __global__ void __launch_bounds__(TTHREADS, 1)
         }
     } else {
         // ---------------------------------------------------- epilogue warps
-        const int ew = warp - 2;  // 0 .. EPI_WARPS-1
+        const int ew = warp - 2;  // 0 .. EW-1
         const int q = warp & 3;   // TMEM lane quarter this warp may access
+        // Warps sharing a quarter split the tile's columns into EW/4 slices.
+        constexpr int SLICE = BN / (EW / 4);
+        const int c_lo = (ew >> 2) * SLICE;
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         uint8_t* etile = smem + tc_epi_off<BN, STAGES>() + ew * 2 * EPI_BUF_BYTES;
         uint64_t* rb = rbar + 2 * ew;
@@ -287,15 +295,15 @@ __global__ void __launch_bounds__(TTHREADS, 1)
             if (args.epi_tma) {
                 const int W = args.out16 ? 64 : 32;  // columns per 128-byte chunk
 #pragma unroll 1
-                for (int c = 0; c < BN; c += W) {
+                for (int c = c_lo; c < c_lo + SLICE; c += W) {
                     uint32_t v[64];
                     tmem_ld_32x32b_x32(tbase + c, *reinterpret_cast<uint32_t(*)[32]>(v));
                     if (W == 64)
                         tmem_ld_32x32b_x32(tbase + c + 32,
                                            *reinterpret_cast<uint32_t(*)[32]>(v + 32));
                     tmem_ld_wait();
-                    if (c + W >= BN) {
-                        // All of this accumulator is in registers: hand it back.
+                    if (c + W >= c_lo + SLICE) {
+                        // This warp's part of the accumulator is in registers: release it.
                         tc_fence_before();
                         mbar_arrive(smem_u32(&tempty[buf]));
                     }
@@ -431,11 +439,11 @@ __global__ void __launch_bounds__(TTHREADS, 1)
                 }
             } else {
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = c_lo / 32; c < (c_lo + SLICE) / 32; ++c) {
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c * 32), r);
                     tmem_ld_wait();
-                    if (c == BN / 32 - 1) {
+                    if (c == (c_lo + SLICE) / 32 - 1) {
                         // All of this buffer is in registers: hand it back to the MMA warp.
                         tc_fence_before();
                         mbar_arrive(smem_u32(&tempty[buf]));
@@ -464,7 +472,7 @@ __global__ void __launch_bounds__(TTHREADS, 1)
     }
 }
 
-template <int BN, int STAGES, bool B_KN>
+template <int BN, int STAGES, bool B_KN, int EW>
 cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& tmA,
                         const CUtensorMap& tmB, const TcEpiMaps* em, const Shape& s,
                         const EpiParams& e, const LaunchCtx& lc) {
@@ -499,30 +507,37 @@ cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& 
     a.status = lc.status;
     a.timeout_ns = lc.timeout_ns;
     a.flags = lc.flags;
-    const int smem = tc_smem_total<BN, STAGES>();
-    auto kern = tc_gemm_kernel<BN, STAGES, B_KN>;
+    const int smem = tc_smem_total<BN, STAGES, EW>();
+    auto kern = tc_gemm_kernel<BN, STAGES, B_KN, EW>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     int64_t grid = cfg.num_ctas > 0 ? cfg.num_ctas : lc.num_sms;
     if (grid > a.total_tiles) grid = a.total_tiles;
     if (grid < 1) grid = 1;
-    kern<<<static_cast<unsigned>(grid), TTHREADS, smem, lc.stream>>>(
+    kern<<<static_cast<unsigned>(grid), tc_threads<EW>(), smem, lc.stream>>>(
         tmA, tmB, em ? em->c : unused_map, (em && em->r_tma) ? em->r : unused_map, a);
     return cudaGetLastError();
 }
+
+// Instantiated configurations: (BN, STAGES, epilogue warps).  Eight epilogue
+// warps (variant 1) take 64 KB of staging tiles, so they pair with fewer stages.
+#define G13_TC_CONFIGS(X) \
+    X(256, 4, 4, 0)       \
+    X(256, 3, 4, 0)       \
+    X(128, 6, 4, 0)       \
+    X(128, 4, 4, 0)       \
+    X(256, 3, 8, 1)       \
+    X(128, 4, 8, 1)
 
 template <bool B_KN>
 cudaError_t launch_tc_layout(const gemm_config_t& cfg, int dtype, const CUtensorMap& tmA,
                              const CUtensorMap& tmB, const TcEpiMaps* em, const Shape& s,
                              const EpiParams& e, const LaunchCtx& lc) {
-    if (cfg.bn == 256 && cfg.stages == 4)
-        return launch_tc_t<256, 4, B_KN>(cfg, dtype, tmA, tmB, em, s, e, lc);
-    if (cfg.bn == 256 && cfg.stages == 3)
-        return launch_tc_t<256, 3, B_KN>(cfg, dtype, tmA, tmB, em, s, e, lc);
-    if (cfg.bn == 128 && cfg.stages == 6)
-        return launch_tc_t<128, 6, B_KN>(cfg, dtype, tmA, tmB, em, s, e, lc);
-    if (cfg.bn == 128 && cfg.stages == 4)
-        return launch_tc_t<128, 4, B_KN>(cfg, dtype, tmA, tmB, em, s, e, lc);
+#define G13_TC_LAUNCH(BN, ST, EW, VAR)                                                   \
+    if (cfg.bn == BN && cfg.stages == ST && cfg.variant == VAR)                          \
+        return launch_tc_t<BN, ST, B_KN, EW>(cfg, dtype, tmA, tmB, em, s, e, lc);
+    G13_TC_CONFIGS(G13_TC_LAUNCH)
+#undef G13_TC_LAUNCH
     return cudaErrorInvalidValue;
 }
 
@@ -530,10 +545,10 @@ cudaError_t launch_tc_layout(const gemm_config_t& cfg, int dtype, const CUtensor
 
 size_t tc_smem_bytes(const gemm_config_t& cfg) {
     if (cfg.bm != TBM || cfg.bk != TBK) return 0;
-    if (cfg.bn == 256 && cfg.stages == 4) return tc_smem_total<256, 4>();
-    if (cfg.bn == 256 && cfg.stages == 3) return tc_smem_total<256, 3>();
-    if (cfg.bn == 128 && cfg.stages == 6) return tc_smem_total<128, 6>();
-    if (cfg.bn == 128 && cfg.stages == 4) return tc_smem_total<128, 4>();
+#define G13_TC_SMEM(BN, ST, EW, VAR) \
+    if (cfg.bn == BN && cfg.stages == ST && cfg.variant == VAR) return tc_smem_total<BN, ST, EW>();
+    G13_TC_CONFIGS(G13_TC_SMEM)
+#undef G13_TC_SMEM
     return 0;
 }
 
@@ -543,5 +558,7 @@ cudaError_t launch_tc(const gemm_config_t& cfg, int dtype, int b_layout, const C
     if (b_layout == GEMM_B_KN) return launch_tc_layout<true>(cfg, dtype, tmA, tmB, em, s, e, lc);
     return launch_tc_layout<false>(cfg, dtype, tmA, tmB, em, s, e, lc);
 }
+
+#undef G13_TC_CONFIGS
 
 }  // namespace g13

@@ -58,10 +58,12 @@ def test_exact_integer(dtype, layout, shape):
 
 
 TC_CONFIGS = [g13.Config("tc", 128, 256, 64, 4), g13.Config("tc", 128, 256, 64, 3),
-              g13.Config("tc", 128, 128, 64, 6), g13.Config("tc", 128, 128, 64, 4)]
+              g13.Config("tc", 128, 128, 64, 6), g13.Config("tc", 128, 128, 64, 4),
+              g13.Config("tc", 128, 256, 64, 3, variant=1),
+              g13.Config("tc", 128, 128, 64, 4, variant=1)]
 
 
-@pytest.mark.parametrize("cfg", TC_CONFIGS, ids=lambda c: f"bn{c.bn}s{c.stages}")
+@pytest.mark.parametrize("cfg", TC_CONFIGS, ids=lambda c: f"bn{c.bn}s{c.stages}v{c.variant}")
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("layout", ["kn", "nk"])
 def test_tc_variants_exact(cfg, dtype, layout):
@@ -73,7 +75,8 @@ def test_tc_variants_exact(cfg, dtype, layout):
     assert np.array_equal(C, cref.reshape(C.shape)), f"{w.name} {cfg}"
     assert run.guard_ok()
     # persistent grid smaller than the tile count: each CTA walks several tiles
-    cfg2 = g13.Config(cfg.kernel, cfg.bm, cfg.bn, cfg.bk, cfg.stages, num_ctas=2)
+    cfg2 = g13.Config(cfg.kernel, cfg.bm, cfg.bn, cfg.bk, cfg.stages, num_ctas=2,
+                      variant=cfg.variant)
     run2 = Run(w, tensors=run.t, config=cfg2)
     C2 = run2.run().result()
     assert np.array_equal(C2, cref.reshape(C.shape)), f"{w.name} {cfg2} (2 CTAs)"
@@ -151,6 +154,9 @@ def test_epilogue_variants(epi, dtype):
         w = Workload(f"epi_{dtype}_{layout}", dtype, 333, 520, 200, b_layout=layout, alpha=0.75,
                      **epi)
         full_check(Run(w, seed=3))
+        if dtype != "f32":
+            # the same epilogue with four epilogue warps (long-K configuration)
+            full_check(Run(w, seed=3, config=g13.Config("tc", 128, 256, 64, 4)))
     # the skinny kernel applies the same epilogue
     w = Workload(f"epi_{dtype}_skinny", dtype, 5, 77, 300, alpha=0.75, **epi)
     full_check(Run(w, seed=4))
