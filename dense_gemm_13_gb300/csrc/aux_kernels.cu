@@ -6,11 +6,19 @@
 // to 16 bytes, and the tensor-core / FFMA kernels read the copy.  The copy is
 // a plain coalesced row-by-row memcpy (HBM-bound).
 //
-// Skinny: for M or N at most 64 a 128-row tensor-core tile would be mostly
+// Skinny: when M or N is tiny a 128-row tensor-core tile would be mostly
 // padding and the GEMM is bound by reading the large operand once ("DeepGEMM",
-// sec. 4.3: a small-block variant for small M or N).  This version gives each
-// warp one output element: lanes stride over K, products accumulate in FP32,
-// and a fixed shuffle tree reduces them (deterministic), then the epilogue.
+// sec. 4.3: a small-block variant for small M or N).  The small operand S
+// (P <= 16 rows per pass) is read through L1; the large one, L, is streamed
+// with 16-byte loads in one of two modes:
+//   dot   L is [Q][K] with K contiguous (A when N is small; B in NK layout
+//         when M is small): a warp walks one row q, lanes split K, and a
+//         shuffle tree reduces the P partial dot products;
+//   axpy  L is [K][Q] with Q contiguous (B in KN layout when M is small): each
+//         thread owns 8 (16-bit) or 4 (FP32) consecutive columns q and walks K.
+// K may be split over several CTAs: each writes FP32 partial sums to the plan
+// workspace and a second kernel adds them in split order (deterministic) and
+// applies the epilogue.  Unaligned operands take scalar loads.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -34,46 +42,176 @@ __global__ void stage_copy_kernel(const T* __restrict__ src, int64_t rows, int64
 }
 
 template <typename T>
-__device__ __forceinline__ float ld_as_float(const T* p);
+__device__ __forceinline__ float to_f(T v);
 template <>
-__device__ __forceinline__ float ld_as_float<float>(const float* p) {
-    return __ldg(p);
+__device__ __forceinline__ float to_f<float>(float v) {
+    return v;
 }
 template <>
-__device__ __forceinline__ float ld_as_float<__half>(const __half* p) {
-    return __half2float(__ldg(p));
+__device__ __forceinline__ float to_f<__half>(__half v) {
+    return __half2float(v);
 }
 template <>
-__device__ __forceinline__ float ld_as_float<__nv_bfloat16>(const __nv_bfloat16* p) {
-    return __bfloat162float(__ldg(p));
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) {
+    return __bfloat162float(v);
 }
 
 template <typename T>
-__global__ void skinny_dot_kernel(const T* __restrict__ A, const T* __restrict__ B, int64_t lda,
-                                  int64_t ldb, int64_t stride_a, int64_t stride_b, int b_nk,
-                                  int64_t M, int64_t N, int64_t K, int64_t batch,
-                                  const EpiParams e) {
+__device__ __forceinline__ float ldf(const T* p) {
+    return to_f<T>(__ldg(p));
+}
+
+// VW consecutive elements (16 bytes) of T as floats; `vec` selects one 16-byte
+// load (aligned, all in range) over scalar loads guarded by `n_valid`.
+template <typename T, int VW>
+__device__ __forceinline__ void load_vec(const T* p, bool vec, int n_valid, float (&out)[VW]) {
+    if (vec) {
+        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p));
+        const T* e = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+        for (int i = 0; i < VW; ++i) out[i] = to_f<T>(e[i]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < VW; ++i) out[i] = i < n_valid ? ldf(p + i) : 0.0f;
+    }
+}
+
+struct SkinnyParams {
+    const void* L;          // large operand
+    int64_t ldl, stride_l;  // row stride ([Q][K] rows in dot mode, [K][Q] rows in axpy mode)
+    const void* S;          // small operand: element (p, k) at S[p*s_sp + k*s_sk]
+    int64_t s_sp, s_sk, stride_s;
+    int64_t P, Q, K, batch;
+    int p_is_m;             // 1: C[p][q];  0: C[q][p]
+    int splits;
+    int64_t kslice;         // K range per split (a multiple of 8)
+    int l_vec, s_vec;       // 16-byte loads allowed for L / S rows
+    float* partial;         // [batch][splits][P][Q] when splits > 1
+    EpiParams e;
+};
+
+__device__ __forceinline__ void skinny_out(const SkinnyParams& sp, int64_t b, int split, int64_t p,
+                                           int64_t q, float v) {
+    if (sp.splits > 1) {
+        sp.partial[((b * sp.splits + split) * sp.P + p) * sp.Q + q] = v;
+    } else if (sp.p_is_m) {
+        epi_store1(sp.e, b, p, q, v);
+    } else {
+        epi_store1(sp.e, b, q, p, v);
+    }
+}
+
+// One warp per (batch, row q, split); lanes split the K range in 16-byte steps.
+// PMAX small-operand rows per pass (1, 4 or 16).
+template <typename T, int PMAX>
+__global__ void __launch_bounds__(256) skinny_dot_kernel(const SkinnyParams sp) {
+    constexpr int VW = 16 / sizeof(T);
     const int lane = threadIdx.x & 31;
-    const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-    const int64_t outputs = M * N * batch;
-    for (int64_t o = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-         o < outputs; o += warps_total) {
-        const int64_t b = o / (M * N);
-        const int64_t r = o - b * M * N;
-        const int64_t m = r / N, n = r - m * N;
-        const T* a = A + b * stride_a + m * lda;
-        const T* bb = B + b * stride_b;
-        float acc = 0.0f;
-        if (b_nk) {
-            const T* bn = bb + n * ldb;
-            for (int64_t k = lane; k < K; k += 32) acc = fmaf(ld_as_float(a + k), ld_as_float(bn + k), acc);
-        } else {
-            for (int64_t k = lane; k < K; k += 32)
-                acc = fmaf(ld_as_float(a + k), ld_as_float(bb + k * ldb + n), acc);
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    const int64_t items = sp.batch * sp.Q * sp.splits;
+    const T* Lbase = static_cast<const T*>(sp.L);
+    const T* Sbase = static_cast<const T*>(sp.S);
+    for (int64_t it = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+         it < items; it += warps) {
+        const int split = static_cast<int>(it % sp.splits);
+        const int64_t bq = it / sp.splits;
+        const int64_t b = bq / sp.Q, q = bq - b * sp.Q;
+        const int64_t k0 = split * sp.kslice;
+        const int64_t k1 = min(sp.K, k0 + sp.kslice);
+        const T* lrow = Lbase + b * sp.stride_l + q * sp.ldl;
+        const T* sb = Sbase + b * sp.stride_s;
+        for (int64_t p0 = 0; p0 < sp.P; p0 += PMAX) {
+            float acc[PMAX];
+#pragma unroll
+            for (int i = 0; i < PMAX; ++i) acc[i] = 0.0f;
+            for (int64_t k = k0 + lane * VW; k < k1; k += 32 * VW) {
+                const int nv = static_cast<int>(min(static_cast<int64_t>(VW), k1 - k));
+                float lv[VW];
+                load_vec<T, VW>(lrow + k, sp.l_vec && nv == VW, nv, lv);
+#pragma unroll
+                for (int i = 0; i < PMAX; ++i) {
+                    if (p0 + i >= sp.P) break;
+                    const T* srow = sb + (p0 + i) * sp.s_sp;
+                    float sv[VW];
+                    if (sp.s_sk == 1) {
+                        load_vec<T, VW>(srow + k, sp.s_vec && nv == VW, nv, sv);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < VW; ++j) sv[j] = j < nv ? ldf(srow + (k + j) * sp.s_sk) : 0.0f;
+                    }
+#pragma unroll
+                    for (int j = 0; j < VW; ++j) acc[i] = fmaf(lv[j], sv[j], acc[i]);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < PMAX; ++i) {
+                if (p0 + i >= sp.P) break;
+                float v = acc[i];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                if (lane == i) skinny_out(sp, b, split, p0 + i, q, v);
+            }
+        }
+    }
+}
+
+// Each thread owns VW consecutive columns q of L = [K][Q] and walks its split's K range.
+template <typename T, int PMAX>
+__global__ void __launch_bounds__(256) skinny_axpy_kernel(const SkinnyParams sp) {
+    constexpr int VW = 16 / sizeof(T);
+    const int64_t q0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * VW;
+    const int split = blockIdx.y;
+    const int64_t b = blockIdx.z;
+    if (q0 >= sp.Q) return;
+    const int nv = static_cast<int>(min(static_cast<int64_t>(VW), sp.Q - q0));
+    const bool vec = sp.l_vec && nv == VW;
+    const int64_t k0 = split * sp.kslice;
+    const int64_t k1 = min(sp.K, k0 + sp.kslice);
+    const T* lcol = static_cast<const T*>(sp.L) + b * sp.stride_l + q0;
+    const T* sb = static_cast<const T*>(sp.S) + b * sp.stride_s;
+    for (int64_t p0 = 0; p0 < sp.P; p0 += PMAX) {
+        float acc[PMAX][VW];
+#pragma unroll
+        for (int i = 0; i < PMAX; ++i)
+#pragma unroll
+            for (int j = 0; j < VW; ++j) acc[i][j] = 0.0f;
+#pragma unroll 2
+        for (int64_t k = k0; k < k1; ++k) {
+            float lv[VW];
+            load_vec<T, VW>(lcol + k * sp.ldl, vec, nv, lv);
+#pragma unroll
+            for (int i = 0; i < PMAX; ++i) {
+                if (p0 + i >= sp.P) break;
+                const float a = ldf(sb + (p0 + i) * sp.s_sp + k * sp.s_sk);
+#pragma unroll
+                for (int j = 0; j < VW; ++j) acc[i][j] = fmaf(a, lv[j], acc[i][j]);
+            }
         }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) epi_store1(e, b, m, n, acc);
+        for (int i = 0; i < PMAX; ++i) {
+            if (p0 + i >= sp.P) break;
+#pragma unroll
+            for (int j = 0; j < VW; ++j)
+                if (j < nv) skinny_out(sp, b, split, p0 + i, q0 + j, acc[i][j]);
+        }
+    }
+}
+
+// Adds the split partial sums in split order and applies the epilogue.
+__global__ void __launch_bounds__(256) skinny_reduce_kernel(const SkinnyParams sp) {
+    const int64_t total = sp.batch * sp.P * sp.Q;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t b = i / (sp.P * sp.Q);
+        const int64_t pq = i - b * sp.P * sp.Q;
+        const int64_t p = pq / sp.Q, q = pq - p * sp.Q;
+        float v = 0.0f;
+        for (int s = 0; s < sp.splits; ++s)
+            v += __ldcg(sp.partial + ((b * sp.splits + s) * sp.P + p) * sp.Q + q);
+        if (sp.p_is_m)
+            epi_store1(sp.e, b, p, q, v);
+        else
+            epi_store1(sp.e, b, q, p, v);
     }
 }
 
@@ -97,34 +235,103 @@ cudaError_t launch_stage_copy(const void* src, int64_t rows, int64_t cols, int64
     return cudaGetLastError();
 }
 
+void skinny_geometry(int64_t M, int64_t N, int b_layout, int64_t* P, int64_t* Q, int* dot) {
+    if (M <= N) {
+        *P = M;
+        *Q = N;
+        *dot = b_layout == GEMM_B_NK;
+    } else {
+        *P = N;
+        *Q = M;
+        *dot = 1;
+    }
+}
+
 cudaError_t launch_skinny(const gemm_config_t& cfg, const SkinnyArgs& a, const Shape& s,
                           const EpiParams& e, const LaunchCtx& lc) {
-    const int64_t outputs = s.M * s.N * s.batch;
-    if (outputs <= 0) return cudaSuccess;
-    const int threads = 256;
-    int64_t blocks = (outputs + 7) / 8;
-    const int64_t cap = static_cast<int64_t>(lc.num_sms > 0 ? lc.num_sms : 148) * 8;
-    if (blocks > cap) blocks = cap;
-    const unsigned grid = static_cast<unsigned>(blocks);
-    const int nk = a.b_layout == GEMM_B_NK;
-    (void)cfg;
-    switch (a.dtype) {
-        case GEMM_F32:
-            skinny_dot_kernel<float><<<grid, threads, 0, lc.stream>>>(
-                static_cast<const float*>(a.A), static_cast<const float*>(a.B), a.lda, a.ldb,
-                a.stride_a, a.stride_b, nk, s.M, s.N, s.K, s.batch, e);
-            break;
-        case GEMM_F16:
-            skinny_dot_kernel<__half><<<grid, threads, 0, lc.stream>>>(
-                static_cast<const __half*>(a.A), static_cast<const __half*>(a.B), a.lda, a.ldb,
-                a.stride_a, a.stride_b, nk, s.M, s.N, s.K, s.batch, e);
-            break;
-        default:
-            skinny_dot_kernel<__nv_bfloat16><<<grid, threads, 0, lc.stream>>>(
-                static_cast<const __nv_bfloat16*>(a.A), static_cast<const __nv_bfloat16*>(a.B),
-                a.lda, a.ldb, a.stride_a, a.stride_b, nk, s.M, s.N, s.K, s.batch, e);
-            break;
+    if (s.M <= 0 || s.N <= 0) return cudaSuccess;
+    SkinnyParams sp{};
+    int dot = 0;
+    skinny_geometry(s.M, s.N, a.b_layout, &sp.P, &sp.Q, &dot);
+    const int esz = a.dtype == GEMM_F32 ? 4 : 2;
+    if (s.M <= s.N) {
+        // small operand A (rows p = m, K contiguous); large operand B
+        sp.S = a.A;
+        sp.s_sp = a.lda;
+        sp.s_sk = 1;
+        sp.stride_s = a.stride_a;
+        sp.L = a.B;
+        sp.ldl = a.ldb;
+        sp.stride_l = a.stride_b;
+        sp.p_is_m = 1;
+    } else {
+        // small operand B^ (rows p = n); large operand A (rows q = m, K contiguous)
+        sp.S = a.B;
+        const bool kn = a.b_layout == GEMM_B_KN;
+        sp.s_sp = kn ? 1 : a.ldb;
+        sp.s_sk = kn ? a.ldb : 1;
+        sp.stride_s = a.stride_b;
+        sp.L = a.A;
+        sp.ldl = a.lda;
+        sp.stride_l = a.stride_a;
+        sp.p_is_m = 0;
     }
+    sp.K = s.K;
+    sp.batch = s.batch;
+    sp.splits = cfg.split_k > 1 ? cfg.split_k : 1;
+    sp.kslice = ((s.K + sp.splits - 1) / sp.splits + 7) / 8 * 8;
+    if (sp.kslice == 0) sp.kslice = 8;
+    sp.partial = sp.splits > 1 ? lc.sk_partials : nullptr;
+    if (sp.splits > 1 && !sp.partial) return cudaErrorInvalidValue;
+    const auto al16 = [](const void* p, int64_t ld, int64_t bs, int64_t batch, int es) {
+        return reinterpret_cast<uintptr_t>(p) % 16 == 0 && (ld * es) % 16 == 0 &&
+               (batch == 1 || (bs * es) % 16 == 0);
+    };
+    sp.l_vec = al16(sp.L, sp.ldl, sp.stride_l, s.batch, esz) ? 1 : 0;
+    sp.s_vec = (sp.s_sk == 1 && al16(sp.S, sp.s_sp, sp.stride_s, s.batch, esz)) ? 1 : 0;
+    sp.e = e;
+    const int sms = lc.num_sms > 0 ? lc.num_sms : 148;
+    const int pm = sp.P == 1 ? 1 : sp.P <= 4 ? 4 : 16;
+    if (dot) {
+        const int64_t items = s.batch * sp.Q * sp.splits;
+        int64_t blocks = (items + 7) / 8;
+        if (blocks > static_cast<int64_t>(sms) * 16) blocks = static_cast<int64_t>(sms) * 16;
+        const unsigned grid = static_cast<unsigned>(blocks > 0 ? blocks : 1);
+#define G13_DOT(T, PM) skinny_dot_kernel<T, PM><<<grid, 256, 0, lc.stream>>>(sp)
+#define G13_DOT_PM(T) \
+    if (pm == 1) G13_DOT(T, 1); else if (pm == 4) G13_DOT(T, 4); else G13_DOT(T, 16)
+        if (a.dtype == GEMM_F32) {
+            G13_DOT_PM(float);
+        } else if (a.dtype == GEMM_F16) {
+            G13_DOT_PM(__half);
+        } else {
+            G13_DOT_PM(__nv_bfloat16);
+        }
+#undef G13_DOT_PM
+#undef G13_DOT
+    } else {
+        const int vw = 16 / esz;
+        const dim3 grid(static_cast<unsigned>((sp.Q + 256 * vw - 1) / (256 * vw)),
+                        static_cast<unsigned>(sp.splits), static_cast<unsigned>(s.batch));
+#define G13_AXPY(T, PM) skinny_axpy_kernel<T, PM><<<grid, 256, 0, lc.stream>>>(sp)
+#define G13_AXPY_PM(T) \
+    if (pm == 1) G13_AXPY(T, 1); else if (pm == 4) G13_AXPY(T, 4); else G13_AXPY(T, 16)
+        if (a.dtype == GEMM_F32) {
+            G13_AXPY_PM(float);
+        } else if (a.dtype == GEMM_F16) {
+            G13_AXPY_PM(__half);
+        } else {
+            G13_AXPY_PM(__nv_bfloat16);
+        }
+#undef G13_AXPY_PM
+#undef G13_AXPY
+    }
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess || sp.splits == 1) return err;
+    const int64_t outs = s.batch * sp.P * sp.Q;
+    int64_t rb = (outs + 255) / 256;
+    if (rb > static_cast<int64_t>(sms) * 8) rb = static_cast<int64_t>(sms) * 8;
+    skinny_reduce_kernel<<<static_cast<unsigned>(rb), 256, 0, lc.stream>>>(sp);
     return cudaGetLastError();
 }
 

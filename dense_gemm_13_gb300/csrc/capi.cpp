@@ -143,10 +143,14 @@ int encode(CUtensorMap* m, int dtype, const void* base, int64_t cols, int64_t ro
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+bool cfg_is_split_skinny(const gemm_config_t& c) {
+    return c.kernel == GEMM_KERNEL_SKINNY && c.split_k > 1;
+}
+
 int kernels_per_run(const gemm_plan_s* pl) {
     const Problem& p = pl->p;
     if (p.M == 0 || p.N == 0) return 0;
-    if (pl->cfg.kernel == GEMM_KERNEL_SKINNY) return 1;
+    if (pl->cfg.kernel == GEMM_KERNEL_SKINNY) return pl->cfg.split_k > 1 ? 2 : 1;
     return 1 + (pl->cfg.stage_a ? 1 : 0) + (pl->cfg.stage_b ? 1 : 0);
 }
 
@@ -195,6 +199,14 @@ int make_plan(const Problem& p, const gemm_config_t* forced, gemm_plan_t* out_pl
         pl->ldb_s = round_up(std::max<int64_t>(g.cols, 1), pad);
         pl->stride_bs = g.rows * pl->ldb_s;
         ws += static_cast<size_t>(round_up(g.batches * pl->stride_bs * esz, 256));
+    }
+    if (cfg.kernel == GEMM_KERNEL_SKINNY && cfg.split_k > 1) {
+        // split-K partial sums: [batch][split_k][P][Q] FP32
+        int64_t P, Q;
+        int dot;
+        skinny_geometry(p.M, p.N, p.epi.b_layout, &P, &Q, &dot);
+        pl->sk_off = ws;
+        ws += static_cast<size_t>(round_up(p.epi.batch * cfg.split_k * P * Q * 4, 256));
     }
     if (cfg.kernel == GEMM_KERNEL_FFMA && cfg.stream_k) {
         // Persistent grid: every CTA the device can hold at once (the launch is
@@ -319,6 +331,8 @@ int gemm_run(gemm_plan_t plan, const void* A, const void* B, void* C, const void
     lc.flags = ep.flags;
     lc.num_sms = plan->num_sms;
     lc.stream = st;
+    if (cfg_is_split_skinny(plan->cfg))
+        lc.sk_partials = reinterpret_cast<float*>(static_cast<char*>(plan->d_ws) + plan->sk_off);
     if (plan->sk_grid > 0) {
         lc.sk_partials = reinterpret_cast<float*>(static_cast<char*>(plan->d_ws) + plan->sk_off);
         lc.sk_tags = reinterpret_cast<unsigned*>(static_cast<char*>(plan->d_ws) + plan->sk_tags_off);
@@ -328,8 +342,8 @@ int gemm_run(gemm_plan_t plan, const void* A, const void* B, void* C, const void
         lc.sk_epoch = ep_tag;
     }
 
-    Shape s{p.M, p.N, p.K, ep.batch, 1, 1};
     const gemm_config_t& cfg = plan->cfg;
+    Shape s{p.M, p.N, p.K, ep.batch, 1, 1};
     cudaError_t ce;
 
     if (cfg.kernel == GEMM_KERNEL_SKINNY) {

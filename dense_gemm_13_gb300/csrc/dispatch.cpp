@@ -4,7 +4,8 @@
 // hit a cached configuration when the same shape comes back, and switch to a
 // small-block kernel when M or N is small.  Buckets here:
 //   * empty problems (M or N = 0) and K = 0, and M or N <= kSkinnyMax:
-//     the memory-bound skinny kernel;
+//     the memory-bound skinny kernel, with K split over CTAs when the large
+//     operand alone would not fill the GPU;
 //   * FP32 inputs: the FFMA kernel, 128x128x32 tiles;
 //   * FP16/BF16 inputs: the tcgen05 kernel, 128 x BN x 64 tiles, BN chosen
 //     between 128 and 256 by the number of waves the tile count needs on
@@ -13,6 +14,7 @@
 #include "dispatch.h"
 
 #include <algorithm>
+#include "internal.h"
 #include <array>
 #include <map>
 #include <mutex>
@@ -20,7 +22,7 @@
 namespace g13 {
 
 namespace {
-constexpr int64_t kSkinnyMax = 8;
+constexpr int64_t kSkinnyMax = 16;
 
 std::mutex g_cache_mu;
 std::map<std::array<int64_t, 19>, gemm_config_t> g_cache;
@@ -93,6 +95,27 @@ static void set_staging(const Problem& p, gemm_config_t* c) {
     if (!stride_tma_ok(p.ldb, p.epi.stride_b, bt, esz)) c->stage_b = 1;
 }
 
+int skinny_splits(const Problem& p, int num_sms) {
+    if (p.M == 0 || p.N == 0 || p.K == 0) return 1;
+    int64_t P, Q;
+    int dot;
+    skinny_geometry(p.M, p.N, p.epi.b_layout, &P, &Q, &dot);
+    const int64_t bt = p.epi.batch;
+    int64_t splits;
+    if (dot) {
+        // one warp per streamed row: aim for ~24 rows in flight per SM, >= 512 K per split
+        splits = cdiv(static_cast<int64_t>(num_sms) * 24, bt * Q);
+        splits = std::min(splits, std::max<int64_t>(1, p.K / 512));
+    } else {
+        // 256 threads x 16 bytes of columns per CTA: aim for ~4 CTAs per SM, >= 64 K per split
+        const int64_t vw = p.dtype == GEMM_F32 ? 4 : 8;
+        const int64_t ctas = cdiv(Q, 256 * vw) * bt;
+        splits = cdiv(static_cast<int64_t>(num_sms) * 4, ctas);
+        splits = std::min(splits, std::max<int64_t>(1, p.K / 64));
+    }
+    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(splits, 1024)));
+}
+
 int choose_config(const Problem& p, int num_sms, gemm_config_t* out) {
     if (!out) return GEMM_ERR_INVALID_ARG;
     if (num_sms <= 0) num_sms = 1;
@@ -107,6 +130,7 @@ int choose_config(const Problem& p, int num_sms, gemm_config_t* out) {
         c.bk = 32;
         c.stages = 1;
         c.raster_group = 1;
+        c.split_k = skinny_splits(p, num_sms);
         *out = c;
         return GEMM_OK;
     }
@@ -166,7 +190,8 @@ int choose_config(const Problem& p, int num_sms, gemm_config_t* out) {
 int check_config(const Problem& p, const gemm_config_t& in, gemm_config_t* out) {
     gemm_config_t c = in;
     if (c.split_k == 0) c.split_k = 1;
-    if (c.split_k != 1) return GEMM_ERR_UNSUPPORTED;
+    if (c.split_k < 1 || (c.split_k != 1 && c.kernel != GEMM_KERNEL_SKINNY) || c.split_k > 1024)
+        return GEMM_ERR_UNSUPPORTED;
     if (c.num_ctas < 0 || c.raster_group < 0) return GEMM_ERR_INVALID_ARG;
     switch (c.kernel) {
         case GEMM_KERNEL_SKINNY:

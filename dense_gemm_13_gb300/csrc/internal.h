@@ -80,8 +80,13 @@ struct SkinnyArgs {
     int dtype;
     int b_layout;
 };
+// Split partial sums go to lc.sk_partials ([batch][split_k][P][Q] FP32) when
+// cfg.split_k > 1; a second kernel reduces them in order and applies the epilogue.
 cudaError_t launch_skinny(const gemm_config_t& cfg, const SkinnyArgs& a, const Shape& s,
                           const EpiParams& e, const LaunchCtx& lc);
+// Which operand the skinny kernel streams: P = the small dimension, Q = the
+// large one; dot = 1 when the streamed operand has K contiguous.
+void skinny_geometry(int64_t M, int64_t N, int b_layout, int64_t* P, int64_t* Q, int* dot);
 
 // Copies [batch][rows][cols] (row stride ld, batch stride bstride, element
 // size esz) into a dense [batch][rows][dst_ld] buffer.  Padding columns are

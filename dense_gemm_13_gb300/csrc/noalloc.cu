@@ -148,6 +148,7 @@ extern "C" int gemm_run_noalloc(gemm_dtype_t dtype, int64_t M, int64_t N, int64_
     rc = choose_config(p, sms, &cfg);  // no cache: nothing is allocated, not even on the host
     if (rc != GEMM_OK) return rc;
     cfg.stream_k = 0;  // whole tiles per CTA: stream-K partial slots would need more scratch
+    cfg.split_k = 1;   // the skinny kernel runs K unsplit (no partial sums to keep)
     const int esz = dtype_size(p.dtype);
     // Misaligned base pointers are staged too (the scratch is always there).
     if (cfg.kernel != GEMM_KERNEL_SKINNY) {

@@ -123,15 +123,36 @@ def test_ffma_stream_k_random_batched():
     full_check(run)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_skinny_forced_exact(dtype):
+SKINNY_CASES = [(1, 300, 777, "kn"), (1, 300, 777, "nk"), (300, 1, 777, "kn"), (300, 1, 777, "nk"),
+                (5, 333, 1000, "kn"), (5, 333, 1000, "nk"), (333, 3, 500, "kn"), (16, 130, 65, "kn"),
+                (17, 90, 333, "kn"), (40, 70, 129, "nk"), (1, 1, 4097, "kn"), (3, 4100, 64, "kn")]
+
+
+@pytest.mark.parametrize("split", [1, 3, 8])
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("case", SKINNY_CASES, ids=lambda c: f"{c[0]}x{c[1]}x{c[2]}-{c[3]}")
+def test_skinny_exact(case, dtype, split):
+    # the memory-bound kernel in both modes (dot: K-contiguous rows streamed,
+    # axpy: N-contiguous columns streamed), with K split over CTAs and the
+    # partial sums added in order by a second kernel
+    M, N, K, layout = case
+    w = _int_workload(dtype, layout, M, N, K)
+    run = Run(w, config=g13.Config("skinny", split_k=split))
+    assert run.info["kernels_per_run"] == (2 if split > 1 else 1)
+    C = run.run().result()
+    _, cref, _ = run.oracle()
+    assert np.array_equal(C, cref.reshape(C.shape)), f"{w.name} split {split}"
+    assert run.guard_ok()
+
+
+def test_skinny_batched_and_epilogue():
     for layout in ("kn", "nk"):
-        w = _int_workload(dtype, layout, 70, 90, 333)
-        run = Run(w, config=g13.Config("skinny"))
-        C = run.run().result()
-        _, cref, _ = run.oracle()
-        assert np.array_equal(C, cref.reshape(C.shape))
-        assert run.guard_ok()
+        w = Workload(f"skinny_b_{layout}", "bf16", 4, 1000, 900, batch=3, b_layout=layout,
+                     bias=True, act="gelu", residual=True, beta=0.5, alpha=0.25)
+        full_check(Run(w, config=g13.Config("skinny", split_k=4)))
+        full_check(Run(w))                                   # dispatcher's choice
+    w = Workload("skinny_nsmall", "f32", 700, 2, 3000, batch=2, bias=True, residual=True)
+    full_check(Run(w))
 
 
 # ---------------------------------------------------------------- epilogues
