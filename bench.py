@@ -47,6 +47,7 @@ def parse():
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the ragged-sweep bucket summary")
     return ap.parse_args()
 
 
@@ -281,6 +282,69 @@ def roofline_for(w, kernel, ms, pk, pk_kind):
             "unit": "TFLOP/s", "peak_source": f"{pk_kind} bf16_tflops (burst; fp16 nominal rate = bf16)"}
 
 
+def sweep_summary(g13, torch, device, pk, pk_kind, reps=8):
+    """Times all 343 ragged sweep triples (BF16, C = 0.5 AB + R) and summarises per bucket.
+
+    Buckets by the dispatcher's kernel and regime: skinny (M or N <= 16), tensor-core
+    problems that are HBM-bound by their arithmetic intensity, and compute-bound ones.
+    Each triple: 2 warm-up runs, then `reps` runs each between an L2 flush and a CUDA
+    event pair; median time.  Roofline fraction as in the main line.
+    """
+    from dense_gemm_13_gb300.inputs import SWEEP_SIZES, sweep_workload
+    big = max(SWEEP_SIZES)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(0)
+    Ab = (torch.rand((big, big), generator=gen, device=device) * 2 - 1).to(torch.bfloat16)
+    Bb = (torch.rand((big, big), generator=gen, device=device) * 2 - 1).to(torch.bfloat16)
+    Rb = torch.rand((big, big), generator=gen, device=device) * 2 - 1
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream()
+    rows = []
+    for M in SWEEP_SIZES:
+        for N in SWEEP_SIZES:
+            for K in SWEEP_SIZES:
+                w = sweep_workload(M, N, K)
+                A = Ab[:M, :K].contiguous()
+                B = Bb[:K, :N].contiguous()
+                R = Rb[:M, :N].contiguous()
+                C = torch.empty((M, N), dtype=torch.float32, device=device)
+                plan = make_plan(g13, w)
+                kern = plan.info()["config"].kernel
+                ts = []
+                for i in range(2 + reps):
+                    flush.fill_(float(i))
+                    s0 = torch.cuda.Event(enable_timing=True)
+                    s1 = torch.cuda.Event(enable_timing=True)
+                    s0.record(stream)
+                    g13.gemm_run(plan, A, B, C, None, R, w.alpha)
+                    s1.record(stream)
+                    if i >= 2:
+                        ts.append((s0, s1))
+                torch.cuda.synchronize()
+                ms = statistics.median(a.elapsed_time(b) for a, b in ts)
+                r = roofline_for(w, kern, ms, pk, pk_kind)
+                if kern == "skinny" or min(M, N) <= 16:
+                    bucket = "skinny"
+                elif r["bound"] == "hbm":
+                    bucket = "tc_hbm_bound"
+                else:
+                    bucket = "tc_compute_bound"
+                rows.append((bucket, w.flops / (ms * 1e-3) / 1e12, r["achieved"] / r["peak"], ms))
+                del plan, A, B, R, C
+    out = {}
+    for bucket in ("skinny", "tc_hbm_bound", "tc_compute_bound"):
+        sel = [x for x in rows if x[0] == bucket]
+        if not sel:
+            continue
+        out[bucket] = {"triples": len(sel),
+                       "median_tflops": round(statistics.median(x[1] for x in sel), 3),
+                       "median_frac": round(statistics.median(x[2] for x in sel), 4),
+                       "min_frac": round(min(x[2] for x in sel), 4),
+                       "max_frac": round(max(x[2] for x in sel), 4)}
+    out["total_ms"] = round(sum(x[3] for x in rows), 3)
+    return out
+
+
 def cpu_baseline(w, host, budget_s=12.0):
     """The FP64 oracle, as it stands, on sampled rows of the workload (host cores)."""
     import numpy as np
@@ -392,6 +456,8 @@ def run_ours(args):
             del dx, Cx, px
             torch.cuda.empty_cache()
         result["secondary"] = extra
+    if not args.no_sweep and ws == 1:
+        result["sweep"] = sweep_summary(g13, torch, device, pk, pk_kind)
     if rank == 0 and ws == 1 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(w, host)
     if rank == 0:

@@ -17,8 +17,10 @@
 //   axpy  L is [K][Q] with Q contiguous (B in KN layout when M is small): each
 //         thread owns 8 (16-bit) or 4 (FP32) consecutive columns q and walks K.
 // K may be split over several CTAs: each writes FP32 partial sums to the plan
-// workspace and a second kernel adds them in split order (deterministic) and
-// applies the epilogue.  Unaligned operands take scalar loads.
+// workspace and counts its arrival on an atomic counter per output group; the
+// CTA (or warp) that arrives last adds the partials in split order
+// (deterministic), applies the epilogue and resets the counter -- no second
+// launch and no waiting.  Unaligned operands take scalar loads.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -61,6 +63,27 @@ __device__ __forceinline__ float ldf(const T* p) {
     return to_f<T>(__ldg(p));
 }
 
+// 16 raw bytes (VW elements of T): one 16-byte load when `vec` (aligned, all in
+// range), else up to n_valid element loads (zero-filled).  Kept raw so that
+// several loads can be in flight before any conversion.
+template <typename T, int VW>
+__device__ __forceinline__ uint4 load_raw(const T* p, bool vec, int n_valid) {
+    if (vec) return __ldg(reinterpret_cast<const uint4*>(p));
+    uint4 r = make_uint4(0, 0, 0, 0);
+    T* e = reinterpret_cast<T*>(&r);
+#pragma unroll
+    for (int i = 0; i < VW; ++i)
+        if (i < n_valid) e[i] = __ldg(p + i);
+    return r;
+}
+
+template <typename T, int VW>
+__device__ __forceinline__ void raw_to_f(const uint4& r, float (&out)[VW]) {
+    const T* e = reinterpret_cast<const T*>(&r);
+#pragma unroll
+    for (int i = 0; i < VW; ++i) out[i] = to_f<T>(e[i]);
+}
+
 // VW consecutive elements (16 bytes) of T as floats; `vec` selects one 16-byte
 // load (aligned, all in range) over scalar loads guarded by `n_valid`.
 template <typename T, int VW>
@@ -87,8 +110,36 @@ struct SkinnyParams {
     int64_t kslice;         // K range per split (a multiple of 8)
     int l_vec, s_vec;       // 16-byte loads allowed for L / S rows
     float* partial;         // [batch][splits][P][Q] when splits > 1
+    unsigned* arrive;       // split arrival counters (zero between launches)
     EpiParams e;
 };
+
+// Sum of the split partials of output (p, q) in split order.
+__device__ __forceinline__ float split_sum(const SkinnyParams& sp, int64_t b, int64_t p,
+                                           int64_t q) {
+    const int64_t slab = sp.P * sp.Q;
+    const float* src = sp.partial + b * sp.splits * slab + p * sp.Q + q;
+    float y = 0.0f;
+    int s = 0;
+    for (; s + 4 <= sp.splits; s += 4) {  // four loads in flight, added in order
+        const float x0 = __ldcg(src + s * slab), x1 = __ldcg(src + (s + 1) * slab);
+        const float x2 = __ldcg(src + (s + 2) * slab), x3 = __ldcg(src + (s + 3) * slab);
+        y += x0;
+        y += x1;
+        y += x2;
+        y += x3;
+    }
+    for (; s < sp.splits; ++s) y += __ldcg(src + s * slab);
+    return y;
+}
+
+__device__ __forceinline__ void skinny_final(const SkinnyParams& sp, int64_t b, int64_t p,
+                                             int64_t q, float v) {
+    if (sp.p_is_m)
+        epi_store1(sp.e, b, p, q, v);
+    else
+        epi_store1(sp.e, b, q, p, v);
+}
 
 __device__ __forceinline__ void skinny_out(const SkinnyParams& sp, int64_t b, int split, int64_t p,
                                            int64_t q, float v) {
@@ -104,7 +155,7 @@ __device__ __forceinline__ void skinny_out(const SkinnyParams& sp, int64_t b, in
 // One warp per (batch, row q, split); lanes split the K range in 16-byte steps.
 // PMAX small-operand rows per pass (1, 4 or 16).
 template <typename T, int PMAX>
-__global__ void __launch_bounds__(256) skinny_dot_kernel(const SkinnyParams sp) {
+__global__ void __launch_bounds__(256, PMAX == 1 ? 3 : 2) skinny_dot_kernel(const SkinnyParams sp) {
     constexpr int VW = 16 / sizeof(T);
     const int lane = threadIdx.x & 31;
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
@@ -120,27 +171,42 @@ __global__ void __launch_bounds__(256) skinny_dot_kernel(const SkinnyParams sp) 
         const int64_t k1 = min(sp.K, k0 + sp.kslice);
         const T* lrow = Lbase + b * sp.stride_l + q * sp.ldl;
         const T* sb = Sbase + b * sp.stride_s;
+        // U 16-byte loads of the streamed row in flight per lane (fewer when P is large)
+        constexpr int U = PMAX == 1 ? 8 : PMAX == 4 ? 4 : 2;
         for (int64_t p0 = 0; p0 < sp.P; p0 += PMAX) {
             float acc[PMAX];
 #pragma unroll
             for (int i = 0; i < PMAX; ++i) acc[i] = 0.0f;
-            for (int64_t k = k0 + lane * VW; k < k1; k += 32 * VW) {
-                const int nv = static_cast<int>(min(static_cast<int64_t>(VW), k1 - k));
-                float lv[VW];
-                load_vec<T, VW>(lrow + k, sp.l_vec && nv == VW, nv, lv);
+            for (int64_t kb = k0 + lane * VW; kb < k1; kb += 32 * VW * U) {
+                uint4 raw[U];
 #pragma unroll
-                for (int i = 0; i < PMAX; ++i) {
-                    if (p0 + i >= sp.P) break;
-                    const T* srow = sb + (p0 + i) * sp.s_sp;
-                    float sv[VW];
-                    if (sp.s_sk == 1) {
-                        load_vec<T, VW>(srow + k, sp.s_vec && nv == VW, nv, sv);
-                    } else {
+                for (int u = 0; u < U; ++u) {
+                    const int64_t k = kb + u * 32 * VW;
+                    const int nv = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(VW), k1 - k)));
+                    raw[u] = load_raw<T, VW>(lrow + k, sp.l_vec && nv == VW, nv);
+                }
 #pragma unroll
-                        for (int j = 0; j < VW; ++j) sv[j] = j < nv ? ldf(srow + (k + j) * sp.s_sk) : 0.0f;
+                for (int u = 0; u < U; ++u) {
+                    const int64_t k = kb + u * 32 * VW;
+                    const int nv = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(VW), k1 - k)));
+                    if (nv == 0) break;
+                    float lvu[VW];
+                    raw_to_f<T, VW>(raw[u], lvu);
+#pragma unroll
+                    for (int i = 0; i < PMAX; ++i) {
+                        if (p0 + i >= sp.P) break;
+                        const T* srow = sb + (p0 + i) * sp.s_sp;
+                        float sv[VW];
+                        if (sp.s_sk == 1) {
+                            load_vec<T, VW>(srow + k, sp.s_vec && nv == VW, nv, sv);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < VW; ++j)
+                                sv[j] = j < nv ? ldf(srow + (k + j) * sp.s_sk) : 0.0f;
+                        }
+#pragma unroll
+                        for (int j = 0; j < VW; ++j) acc[i] = fmaf(lvu[j], sv[j], acc[i]);
                     }
-#pragma unroll
-                    for (int j = 0; j < VW; ++j) acc[i] = fmaf(lv[j], sv[j], acc[i]);
                 }
             }
 #pragma unroll
@@ -152,66 +218,184 @@ __global__ void __launch_bounds__(256) skinny_dot_kernel(const SkinnyParams sp) 
                 if (lane == i) skinny_out(sp, b, split, p0 + i, q, v);
             }
         }
+        if (sp.splits > 1) {
+            // The warp that finishes row (b, q) last adds all splits' partials.
+            __threadfence();
+            __syncwarp();
+            unsigned last = 0;
+            if (lane == 0) last = atomicAdd(sp.arrive + b * sp.Q + q, 1u) == static_cast<unsigned>(sp.splits - 1);
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (last) {
+                __threadfence();
+                for (int64_t p = lane; p < sp.P; p += 32) skinny_final(sp, b, p, q, split_sum(sp, b, p, q));
+                if (lane == 0) sp.arrive[b * sp.Q + q] = 0u;
+            }
+        }
     }
 }
 
-// Each thread owns VW consecutive columns q of L = [K][Q] and walks its split's K range.
+// Each CTA owns CW = 32 x VW consecutive columns q of L = [K][Q] (lane l the VW
+// columns at q0 + l*VW, loaded as one 16-byte vector per row); its 8 warps take
+// interleaved groups of G = VW rows of the split's K range, so every warp reads
+// whole 512-byte row segments, and their sums are added in warp order through
+// shared memory (deterministic).
 template <typename T, int PMAX>
-__global__ void __launch_bounds__(256) skinny_axpy_kernel(const SkinnyParams sp) {
+__global__ void __launch_bounds__(256, PMAX == 1 ? 3 : PMAX == 4 ? 2 : 1)
+    skinny_axpy_kernel(const SkinnyParams sp) {
     constexpr int VW = 16 / sizeof(T);
-    const int64_t q0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * VW;
+    constexpr int CW = 32 * VW;
+    constexpr int G = VW;
+    __shared__ float red[8][CW];
+    __shared__ unsigned s_last;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t qb = static_cast<int64_t>(blockIdx.x) * CW;
+    const int64_t q0 = qb + lane * VW;
     const int split = blockIdx.y;
     const int64_t b = blockIdx.z;
-    if (q0 >= sp.Q) return;
-    const int nv = static_cast<int>(min(static_cast<int64_t>(VW), sp.Q - q0));
+    const bool active = q0 < sp.Q;
+    const int nv = active ? static_cast<int>(min(static_cast<int64_t>(VW), sp.Q - q0)) : 0;
     const bool vec = sp.l_vec && nv == VW;
     const int64_t k0 = split * sp.kslice;
     const int64_t k1 = min(sp.K, k0 + sp.kslice);
     const T* lcol = static_cast<const T*>(sp.L) + b * sp.stride_l + q0;
     const T* sb = static_cast<const T*>(sp.S) + b * sp.stride_s;
+    const bool s_vec = sp.s_vec && sp.s_sk == 1;
     for (int64_t p0 = 0; p0 < sp.P; p0 += PMAX) {
         float acc[PMAX][VW];
 #pragma unroll
         for (int i = 0; i < PMAX; ++i)
 #pragma unroll
             for (int j = 0; j < VW; ++j) acc[i][j] = 0.0f;
-#pragma unroll 2
-        for (int64_t k = k0; k < k1; ++k) {
-            float lv[VW];
-            load_vec<T, VW>(lcol + k * sp.ldl, vec, nv, lv);
+        // A group's G streamed rows are in flight together before any
+        // conversion; one 16-byte load of each small-operand row covers the
+        // group when K is contiguous there.
+        for (int64_t kb = k0 + warp * G; active && kb < k1; kb += 8 * G) {
+            const int gn = static_cast<int>(min(static_cast<int64_t>(G), k1 - kb));
+            uint4 raw[G];
+#pragma unroll
+            for (int u = 0; u < G; ++u)
+                if (u < gn) raw[u] = load_raw<T, VW>(lcol + (kb + u) * sp.ldl, vec, nv);
 #pragma unroll
             for (int i = 0; i < PMAX; ++i) {
                 if (p0 + i >= sp.P) break;
-                const float a = ldf(sb + (p0 + i) * sp.s_sp + k * sp.s_sk);
+                const T* srow = sb + (p0 + i) * sp.s_sp;
+                float a[G];
+                if (s_vec && gn == G && (kb & (G - 1)) == 0) {
+                    raw_to_f<T, VW>(__ldg(reinterpret_cast<const uint4*>(srow + kb)), a);
+                } else {
 #pragma unroll
-                for (int j = 0; j < VW; ++j) acc[i][j] = fmaf(a, lv[j], acc[i][j]);
+                    for (int u = 0; u < G; ++u) a[u] = u < gn ? ldf(srow + (kb + u) * sp.s_sk) : 0.0f;
+                }
+#pragma unroll
+                for (int u = 0; u < G; ++u) {
+                    if (u >= gn) break;
+                    float lv[VW];
+                    raw_to_f<T, VW>(raw[u], lv);
+#pragma unroll
+                    for (int j = 0; j < VW; ++j) acc[i][j] = fmaf(a[u], lv[j], acc[i][j]);
+                }
             }
         }
+        // add the 8 warps' sums column by column, in warp order
 #pragma unroll
         for (int i = 0; i < PMAX; ++i) {
             if (p0 + i >= sp.P) break;
+            __syncthreads();
 #pragma unroll
-            for (int j = 0; j < VW; ++j)
-                if (j < nv) skinny_out(sp, b, split, p0 + i, q0 + j, acc[i][j]);
+            for (int j = 0; j < VW; ++j) red[warp][lane * VW + j] = acc[i][j];
+            __syncthreads();
+            for (int c = threadIdx.x; c < CW; c += 256) {
+                if (qb + c >= sp.Q) break;
+                float v = red[0][c];
+#pragma unroll
+                for (int w = 1; w < 8; ++w) v += red[w][c];
+                skinny_out(sp, b, split, p0 + i, qb + c, v);
+            }
+        }
+    }
+    if (sp.splits > 1) {
+        // The CTA that finishes this column block last adds all splits' partials.
+        __threadfence();
+        __syncthreads();
+        unsigned* ctr = sp.arrive + b * gridDim.x + blockIdx.x;
+        if (threadIdx.x == 0) s_last = atomicAdd(ctr, 1u) == static_cast<unsigned>(sp.splits - 1);
+        __syncthreads();
+        if (s_last) {
+            __threadfence();
+            for (int64_t p = 0; p < sp.P; ++p)
+                for (int c = threadIdx.x; c < CW; c += 256) {
+                    if (qb + c >= sp.Q) break;
+                    skinny_final(sp, b, p, qb + c, split_sum(sp, b, p, qb + c));
+                }
+            if (threadIdx.x == 0) *ctr = 0u;
         }
     }
 }
 
-// Adds the split partial sums in split order and applies the epilogue.
+// Adds the split partial sums and applies the epilogue.  With few splits each
+// thread owns one output and sums its splits in order (loads in flight four at
+// a time).  With many splits (> 16) a block covers 32 consecutive outputs: its 8
+// warps each sum an interleaved subset of the splits (warp w takes w, w+8, ...)
+// in order and warp 0 adds the 8 subtotals in warp order.  Both orders are
+// fixed, so results are run-to-run identical.
+__device__ __forceinline__ void reduce_store(const SkinnyParams& sp, int64_t i, float y) {
+    const int64_t b = i / (sp.P * sp.Q);
+    const int64_t pq = i - b * sp.P * sp.Q;
+    const int64_t p = pq / sp.Q, q = pq - p * sp.Q;
+    if (sp.p_is_m)
+        epi_store1(sp.e, b, p, q, y);
+    else
+        epi_store1(sp.e, b, q, p, y);
+}
+
 __global__ void __launch_bounds__(256) skinny_reduce_kernel(const SkinnyParams sp) {
     const int64_t total = sp.batch * sp.P * sp.Q;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t b = i / (sp.P * sp.Q);
-        const int64_t pq = i - b * sp.P * sp.Q;
-        const int64_t p = pq / sp.Q, q = pq - p * sp.Q;
+    const int64_t slab = sp.P * sp.Q;
+    if (sp.splits <= 16) {
+        for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+             i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+            const int64_t b = i / slab;
+            const float* src = sp.partial + b * sp.splits * slab + (i - b * slab);
+            float x[16];
+#pragma unroll
+            for (int s = 0; s < 16; ++s) x[s] = s < sp.splits ? __ldcg(src + s * slab) : 0.0f;
+            float y = 0.0f;
+#pragma unroll
+            for (int s = 0; s < 16; ++s)
+                if (s < sp.splits) y += x[s];
+            reduce_store(sp, i, y);
+        }
+        return;
+    }
+    __shared__ float part[8][33];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * 32; base < total;
+         base += static_cast<int64_t>(gridDim.x) * 32) {
+        const int64_t i = base + lane;
         float v = 0.0f;
-        for (int s = 0; s < sp.splits; ++s)
-            v += __ldcg(sp.partial + ((b * sp.splits + s) * sp.P + p) * sp.Q + q);
-        if (sp.p_is_m)
-            epi_store1(sp.e, b, p, q, v);
-        else
-            epi_store1(sp.e, b, q, p, v);
+        if (i < total) {
+            const int64_t b = i / slab;
+            const float* src = sp.partial + b * sp.splits * slab + (i - b * slab);
+            int s = w;
+            for (; s + 24 < sp.splits; s += 32) {  // four loads in flight, summed in order
+                const float x0 = __ldcg(src + s * slab), x1 = __ldcg(src + (s + 8) * slab);
+                const float x2 = __ldcg(src + (s + 16) * slab), x3 = __ldcg(src + (s + 24) * slab);
+                v += x0;
+                v += x1;
+                v += x2;
+                v += x3;
+            }
+            for (; s < sp.splits; s += 8) v += __ldcg(src + s * slab);
+        }
+        part[w][lane] = v;
+        __syncthreads();
+        if (w == 0 && i < total) {
+            float y = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) y += part[k][lane];
+            reduce_store(sp, i, y);
+        }
+        __syncthreads();
     }
 }
 
@@ -282,7 +466,8 @@ cudaError_t launch_skinny(const gemm_config_t& cfg, const SkinnyArgs& a, const S
     sp.kslice = ((s.K + sp.splits - 1) / sp.splits + 7) / 8 * 8;
     if (sp.kslice == 0) sp.kslice = 8;
     sp.partial = sp.splits > 1 ? lc.sk_partials : nullptr;
-    if (sp.splits > 1 && !sp.partial) return cudaErrorInvalidValue;
+    sp.arrive = sp.splits > 1 ? lc.sk_tags : nullptr;
+    if (sp.splits > 1 && (!sp.partial || !sp.arrive)) return cudaErrorInvalidValue;
     const auto al16 = [](const void* p, int64_t ld, int64_t bs, int64_t batch, int es) {
         return reinterpret_cast<uintptr_t>(p) % 16 == 0 && (ld * es) % 16 == 0 &&
                (batch == 1 || (bs * es) % 16 == 0);
@@ -311,7 +496,7 @@ cudaError_t launch_skinny(const gemm_config_t& cfg, const SkinnyArgs& a, const S
 #undef G13_DOT
     } else {
         const int vw = 16 / esz;
-        const dim3 grid(static_cast<unsigned>((sp.Q + 256 * vw - 1) / (256 * vw)),
+        const dim3 grid(static_cast<unsigned>((sp.Q + 32 * vw - 1) / (32 * vw)),
                         static_cast<unsigned>(sp.splits), static_cast<unsigned>(s.batch));
 #define G13_AXPY(T, PM) skinny_axpy_kernel<T, PM><<<grid, 256, 0, lc.stream>>>(sp)
 #define G13_AXPY_PM(T) \
@@ -326,10 +511,23 @@ cudaError_t launch_skinny(const gemm_config_t& cfg, const SkinnyArgs& a, const S
 #undef G13_AXPY_PM
 #undef G13_AXPY
     }
-    cudaError_t err = cudaGetLastError();
-    if (err != cudaSuccess || sp.splits == 1) return err;
-    const int64_t outs = s.batch * sp.P * sp.Q;
-    int64_t rb = (outs + 255) / 256;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_split_reduce(const float* partial, int64_t M, int64_t N, int64_t batch,
+                                int splits, const EpiParams& e, const LaunchCtx& lc) {
+    SkinnyParams sp{};
+    sp.P = M;
+    sp.Q = N;
+    sp.batch = batch;
+    sp.splits = splits;
+    sp.p_is_m = 1;
+    sp.partial = const_cast<float*>(partial);
+    sp.e = e;
+    const int64_t outs = batch * M * N;
+    if (outs <= 0) return cudaSuccess;
+    const int sms = lc.num_sms > 0 ? lc.num_sms : 148;
+    int64_t rb = splits <= 16 ? (outs + 255) / 256 : (outs + 31) / 32;
     if (rb > static_cast<int64_t>(sms) * 8) rb = static_cast<int64_t>(sms) * 8;
     skinny_reduce_kernel<<<static_cast<unsigned>(rb), 256, 0, lc.stream>>>(sp);
     return cudaGetLastError();

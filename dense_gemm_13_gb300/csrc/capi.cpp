@@ -67,7 +67,8 @@ struct gemm_plan_s {
     size_t ws_b_off = 0;
     int64_t lda_s = 0, ldb_s = 0;        // leading dims of the staged copies
     int64_t stride_as = 0, stride_bs = 0;
-    size_t sk_off = 0, sk_tags_off = 0;   // stream-K partial slots and tags in d_ws
+    size_t sk_off = 0, sk_tags_off = 0;   // stream-K / split-K partial slots and tags in d_ws
+    size_t sk_ctr_bytes = 0;              // skinny split-K arrival counters
     int64_t sk_grid = 0;
     std::atomic<unsigned> epoch{0};       // tag counter for stream-K launches
     std::mutex mu;                        // guards the descriptor cache
@@ -78,6 +79,8 @@ struct gemm_plan_s {
     const void* mapR_src = nullptr;
     bool epi_valid = false;
     TcEpiMaps epi{};
+    bool split_map_valid = false;         // split-K partial-slab descriptor (workspace)
+    TcEpiMaps split_map{};
 };
 
 namespace {
@@ -147,11 +150,16 @@ bool cfg_is_split_skinny(const gemm_config_t& c) {
     return c.kernel == GEMM_KERNEL_SKINNY && c.split_k > 1;
 }
 
+int tc_splits_of(const gemm_plan_s* pl) {
+    return pl->cfg.kernel == GEMM_KERNEL_TC ? tc_effective_splits(pl->p.K, pl->cfg.split_k) : 1;
+}
+
 int kernels_per_run(const gemm_plan_s* pl) {
     const Problem& p = pl->p;
     if (p.M == 0 || p.N == 0) return 0;
-    if (pl->cfg.kernel == GEMM_KERNEL_SKINNY) return pl->cfg.split_k > 1 ? 2 : 1;
-    return 1 + (pl->cfg.stage_a ? 1 : 0) + (pl->cfg.stage_b ? 1 : 0);
+    if (pl->cfg.kernel == GEMM_KERNEL_SKINNY) return 1;
+    return 1 + (pl->cfg.stage_a ? 1 : 0) + (pl->cfg.stage_b ? 1 : 0) +
+           (tc_splits_of(pl) > 1 ? 1 : 0);
 }
 
 int make_plan(const Problem& p, const gemm_config_t* forced, gemm_plan_t* out_plan) {
@@ -200,13 +208,24 @@ int make_plan(const Problem& p, const gemm_config_t* forced, gemm_plan_t* out_pl
         pl->stride_bs = g.rows * pl->ldb_s;
         ws += static_cast<size_t>(round_up(g.batches * pl->stride_bs * esz, 256));
     }
+    if (cfg.kernel == GEMM_KERNEL_TC && tc_effective_splits(p.K, cfg.split_k) > 1) {
+        // split-K partial slabs: [batch][splits][M][N] FP32
+        pl->sk_off = ws;
+        ws += static_cast<size_t>(round_up(
+            p.epi.batch * tc_effective_splits(p.K, cfg.split_k) * p.M * p.N * 4, 256));
+    }
     if (cfg.kernel == GEMM_KERNEL_SKINNY && cfg.split_k > 1) {
-        // split-K partial sums: [batch][split_k][P][Q] FP32
+        // split-K partial sums [batch][split_k][P][Q] FP32, then one arrival
+        // counter per output group (at most batch x Q), zeroed here and reset
+        // by the kernel that consumes them
         int64_t P, Q;
         int dot;
         skinny_geometry(p.M, p.N, p.epi.b_layout, &P, &Q, &dot);
         pl->sk_off = ws;
         ws += static_cast<size_t>(round_up(p.epi.batch * cfg.split_k * P * Q * 4, 256));
+        pl->sk_tags_off = ws;
+        pl->sk_ctr_bytes = static_cast<size_t>(round_up(p.epi.batch * Q * 4, 256));
+        ws += pl->sk_ctr_bytes;
     }
     if (cfg.kernel == GEMM_KERNEL_FFMA && cfg.stream_k) {
         // Persistent grid: every CTA the device can hold at once (the launch is
@@ -230,6 +249,8 @@ int make_plan(const Problem& p, const gemm_config_t* forced, gemm_plan_t* out_pl
     if (ce == cudaSuccess && pl->sk_grid > 0)
         ce = cudaMemset(static_cast<char*>(pl->d_ws) + pl->sk_tags_off, 0,
                         static_cast<size_t>(pl->sk_grid) * 4);
+    if (ce == cudaSuccess && pl->sk_ctr_bytes > 0)
+        ce = cudaMemset(static_cast<char*>(pl->d_ws) + pl->sk_tags_off, 0, pl->sk_ctr_bytes);
     if (ce != cudaSuccess) {
         if (pl->d_status) cudaFree(pl->d_status);
         delete pl;
@@ -331,8 +352,10 @@ int gemm_run(gemm_plan_t plan, const void* A, const void* B, void* C, const void
     lc.flags = ep.flags;
     lc.num_sms = plan->num_sms;
     lc.stream = st;
-    if (cfg_is_split_skinny(plan->cfg))
+    if (cfg_is_split_skinny(plan->cfg) || tc_splits_of(plan) > 1)
         lc.sk_partials = reinterpret_cast<float*>(static_cast<char*>(plan->d_ws) + plan->sk_off);
+    if (cfg_is_split_skinny(plan->cfg))
+        lc.sk_tags = reinterpret_cast<unsigned*>(static_cast<char*>(plan->d_ws) + plan->sk_tags_off);
     if (plan->sk_grid > 0) {
         lc.sk_partials = reinterpret_cast<float*>(static_cast<char*>(plan->d_ws) + plan->sk_off);
         lc.sk_tags = reinterpret_cast<unsigned*>(static_cast<char*>(plan->d_ws) + plan->sk_tags_off);
@@ -425,6 +448,44 @@ int gemm_run(gemm_plan_t plan, const void* A, const void* B, void* C, const void
         ce = launch_ffma(cfg, ep.b_layout, mA, mB, s, e, lc);
         return map_cuda_error(ce);
     }
+    const int splits = tc_splits_of(plan);
+    if (splits > 1) {
+        // Split-K: the kernel writes raw FP32 partial slabs [batch][split][M][N]
+        // (through TMA when N allows it), a second kernel adds them and applies e.
+        EpiParams part{};
+        part.C = lc.sk_partials;
+        part.ldc = p.N;
+        part.stride_c = p.M * p.N;
+        part.M = p.M;
+        part.N = p.N;
+        part.alpha = 1.0f;
+        part.beta = 0.0f;
+        part.out_dtype = GEMM_F32;
+        part.act = GEMM_ACT_NONE;
+        part.c_vec = p.N % 4 == 0;
+        TcEpiMaps pm{};
+        bool use_pm = false;
+        const int64_t n_tma = p.N / 4 * 4;
+        if (p.N % 4 == 0 && n_tma > 0) {
+            std::lock_guard<std::mutex> lk(plan->mu);
+            if (!plan->split_map_valid) {
+                plan->split_map_valid =
+                    encode(&plan->split_map.c, GEMM_F32, part.C, n_tma, p.M, p.N,
+                           ep.batch * splits, p.M * p.N, 32u, 32u, CU_TENSOR_MAP_SWIZZLE_128B) ==
+                    GEMM_OK;
+                plan->split_map.n_tma = n_tma;
+                plan->split_map.c_bmul = splits;
+                plan->split_map.c_smul = 1;
+                plan->split_map.r_tma = 0;
+            }
+            if (plan->split_map_valid) {
+                pm = plan->split_map;
+                use_pm = true;
+            }
+        }
+        ce = launch_tc(cfg, p.dtype, ep.b_layout, mA, mB, use_pm ? &pm : nullptr, s, part, lc, &e);
+        return map_cuda_error(ce);
+    }
     // Tensor-core epilogue through TMA when C (and an FP32 residual) allow it:
     // 16-byte-aligned base, row stride and batch stride.
     TcEpiMaps em;
@@ -453,6 +514,7 @@ int gemm_run(gemm_plan_t plan, const void* A, const void* B, void* C, const void
                                 r_shared ? 1 : ep.batch, ep.stride_r, 32u, 32u,
                                 CU_TENSOR_MAP_SWIZZLE_128B);
                 m.c_bmul = ep.batch > 1 ? 1 : 0;
+                m.c_smul = 0;
                 m.r_bmul = (ep.batch > 1 && !r_shared) ? 1 : 0;
                 plan->epi_valid = rc == GEMM_OK;
                 plan->epi = m;

@@ -22,7 +22,11 @@
 namespace g13 {
 
 namespace {
-constexpr int64_t kSkinnyMax = 16;
+// Up to 4 small-operand rows the skinny kernel streams the large operand at
+// HBM speed; beyond that its FMAs per loaded element make it CUDA-core bound
+// (16 rows: 199 us for 16 x 6144 x 6144 BF16) and the tensor cores (with
+// split-K) are faster (17 rows: 39 us).
+constexpr int64_t kSkinnyMax = 4;
 
 std::mutex g_cache_mu;
 std::map<std::array<int64_t, 19>, gemm_config_t> g_cache;
@@ -107,13 +111,54 @@ int skinny_splits(const Problem& p, int num_sms) {
         splits = cdiv(static_cast<int64_t>(num_sms) * 24, bt * Q);
         splits = std::min(splits, std::max<int64_t>(1, p.K / 512));
     } else {
-        // 256 threads x 16 bytes of columns per CTA: aim for ~4 CTAs per SM, >= 64 K per split
+        // a CTA covers 32 x 16 bytes of columns with 8 warps along K: aim for a full
+        // wave at the kernel's occupancy (3 CTAs per SM for one row, else 2) and
+        // at least two row groups per warp
         const int64_t vw = p.dtype == GEMM_F32 ? 4 : 8;
-        const int64_t ctas = cdiv(Q, 256 * vw) * bt;
-        splits = cdiv(static_cast<int64_t>(num_sms) * 4, ctas);
-        splits = std::min(splits, std::max<int64_t>(1, p.K / 64));
+        const int64_t ctas = cdiv(Q, 32 * vw) * bt;
+        splits = cdiv(static_cast<int64_t>(num_sms) * (P == 1 ? 3 : 2), ctas);
+        splits = std::min(splits, std::max<int64_t>(1, p.K / (16 * vw)));
     }
     return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(splits, 1024)));
+}
+
+// Split-K for the tensor-core kernel when its tiles cannot fill the GPU (small
+// M and N, long K): a rough time model -- waves of (tile, split) items, each
+// limited by its MMA work or by the HBM share its SM gets -- plus the partial
+// slabs' write + read and the reduction launch.  Returns 1 when splitting does
+// not pay by at least 10 %.
+int tc_splits(const Problem& p, int num_sms, int bn) {
+    const int64_t M = p.M, N = p.N, K = p.K, bt = p.epi.batch;
+    const int64_t tiles = bt * cdiv(M, 128) * cdiv(N, bn);
+    const int64_t kb = cdiv(K, 64);
+    if (tiles * 2 > num_sms || kb < 4) return 1;
+    const double esz = dtype_size(p.dtype);
+    // rows/columns a tile really reads (TMA zero-fills past the edge without traffic)
+    const double rows = static_cast<double>(std::min<int64_t>(M, 128));
+    const double cols = static_cast<double>(std::min<int64_t>(N, bn));
+    auto model = [&](int64_t s) {
+        const int64_t items = tiles * s;
+        const double kpart = static_cast<double>(cdiv(kb, s)) * 64.0;
+        const double t_mma = 128.0 * bn * kpart * 2.0 / 15e12;  // ~15 TFLOP/s per SM
+        // one SM streams ~80 GB/s; all of them share ~6 TB/s of HBM
+        const double share =
+            std::min(80e9, 6e12 / static_cast<double>(std::min<int64_t>(items, num_sms)));
+        const double t_mem = (rows + cols) * kpart * esz / share;
+        const double waves = static_cast<double>(cdiv(items, num_sms));
+        double t = waves * std::max(t_mma, t_mem);
+        if (s > 1) t += static_cast<double>(s) * M * N * bt * 8.0 / 6e12 + 4e-6;
+        return t;
+    };
+    int best = 1;
+    double best_t = model(1);
+    for (int64_t s = 2; s <= 64 && s <= kb / 2; ++s) {
+        const double t = model(s);
+        if (t < best_t * 0.9) {
+            best_t = t;
+            best = static_cast<int>(s);
+        }
+    }
+    return best;
 }
 
 int choose_config(const Problem& p, int num_sms, gemm_config_t* out) {
@@ -181,6 +226,7 @@ int choose_config(const Problem& p, int num_sms, gemm_config_t* out) {
             c.stages = c.bn == 256 ? 3 : 4;
         }
         c.raster_group = static_cast<int32_t>(std::min<int64_t>(16, mt));
+        c.split_k = tc_splits(p, num_sms, c.bn);
     }
     set_staging(p, &c);
     *out = c;
@@ -190,7 +236,7 @@ int choose_config(const Problem& p, int num_sms, gemm_config_t* out) {
 int check_config(const Problem& p, const gemm_config_t& in, gemm_config_t* out) {
     gemm_config_t c = in;
     if (c.split_k == 0) c.split_k = 1;
-    if (c.split_k < 1 || (c.split_k != 1 && c.kernel != GEMM_KERNEL_SKINNY) || c.split_k > 1024)
+    if (c.split_k < 1 || (c.split_k != 1 && c.kernel == GEMM_KERNEL_FFMA) || c.split_k > 1024)
         return GEMM_ERR_UNSUPPORTED;
     if (c.num_ctas < 0 || c.raster_group < 0) return GEMM_ERR_INVALID_ARG;
     switch (c.kernel) {

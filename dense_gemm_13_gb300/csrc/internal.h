@@ -48,15 +48,24 @@ struct TcEpiMaps {
     CUtensorMap c, r;
     int r_tma;
     int c_bmul, r_bmul;  // batch coordinate multipliers (0: shared across the batch)
+    int c_smul;          // split-K: split coordinate multiplier of the C descriptor
     int64_t n_tma;       // columns covered by the C descriptor (N rounded down to 16 bytes)
 };
 
 // Tensor-core path: A [batch][M][K] 16-bit via tmA (K innermost); B via tmB:
 // NK layout -> dims (K, N, batch), KN layout -> dims (N, K, batch).  With em
-// null the epilogue stores C from registers.
+// null the epilogue stores C from registers.  Split-K (cfg.split_k > 1): `e`
+// describes the FP32 partial slabs [batch][split][M][N] the kernel writes, and
+// final_epi the real epilogue a second kernel applies after adding them.
 cudaError_t launch_tc(const gemm_config_t& cfg, int dtype, int b_layout, const CUtensorMap& tmA,
                       const CUtensorMap& tmB, const TcEpiMaps* em, const Shape& s,
-                      const EpiParams& e, const LaunchCtx& lc);
+                      const EpiParams& e, const LaunchCtx& lc,
+                      const EpiParams* final_epi = nullptr);
+// K ranges a tensor-core split-K launch actually uses (<= split_k, none empty).
+int tc_effective_splits(int64_t K, int split_k);
+// Adds partial slabs [batch][splits][M][N] in split order and applies e.
+cudaError_t launch_split_reduce(const float* partial, int64_t M, int64_t N, int64_t batch,
+                                int splits, const EpiParams& e, const LaunchCtx& lc);
 // Shared memory the TC kernel needs for a config (bytes), or 0 if unsupported.
 size_t tc_smem_bytes(const gemm_config_t& cfg);
 

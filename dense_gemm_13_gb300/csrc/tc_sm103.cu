@@ -57,6 +57,10 @@ struct TcArgs {
     int r_tma;      // 1: the FP32 residual is read by TMA loads (implies epi_tma)
     int out16;      // 1: C holds 16-bit values (64 columns per 128-byte chunk)
     int c_bmul, r_bmul;
+    int c_smul;     // split-K: C batch coordinate = b * c_bmul + split * c_smul
+    int splits;     // split-K: K-block ranges per tile (1 = none)
+    int kb_per_split;
+    int64_t total_items;  // total_tiles * splits (split-major order)
     int bias_vec;   // 1: bias is 16-byte aligned (float4 loads)
     int64_t n_tma;  // columns [0, n_tma) go out by TMA (a multiple of 16 bytes); the rest,
                     // fewer than 16 bytes per row, from registers
@@ -164,19 +168,22 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
             uint32_t ph = 0;
             uint32_t armed = 0, armed_par = 0;  // per stage: armed and not yet seen consumed
             bool ok = true;
-            for (int64_t t = blockIdx.x; ok && t < args.total_tiles; t += gridDim.x) {
+            for (int64_t t = blockIdx.x; ok && t < args.total_items; t += gridDim.x) {
+                const int split = static_cast<int>(t / args.total_tiles);
                 int64_t b, mt, nt;
-                tc_tile_coords(t, args, b, mt, nt);
+                tc_tile_coords(t - split * args.total_tiles, args, b, mt, nt);
                 const int32_t m0 = static_cast<int32_t>(mt * TBM);
                 const int32_t n0 = static_cast<int32_t>(nt * BN);
-                for (int kb = 0; kb < kb_total; ++kb) {
+                const int kb_lo = split * args.kb_per_split;
+                const int kb_hi = min(kb_total, kb_lo + args.kb_per_split);
+                for (int kb = kb_lo; kb < kb_hi; ++kb) {
                     if (!mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1u, abort_flag, args.status,
                                            tmo)) {
                         ok = false;
                         break;
                     }
                     armed &= ~(1u << s);  // the previous use of this stage was consumed
-                    const bool skip = stall && t == blockIdx.x && kb == 0;
+                    const bool skip = stall && t == blockIdx.x && kb == kb_lo;
                     if (!skip) {
                         const uint32_t bar = smem_u32(&full[s]);
                         uint8_t* sa = smem + s * L::STAGE_BYTES;
@@ -216,7 +223,7 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
             bool ok = true;
             bool issued_any = false;
             int lt = 0;
-            for (int64_t t = blockIdx.x; ok && t < args.total_tiles; t += gridDim.x, ++lt) {
+            for (int64_t t = blockIdx.x; ok && t < args.total_items; t += gridDim.x, ++lt) {
                 const int buf = lt & 1;
                 const uint32_t tph = static_cast<uint32_t>(lt >> 1) & 1u;
                 if (!mbar_wait_bounded(smem_u32(&tempty[buf]), tph ^ 1u, abort_flag, args.status,
@@ -226,7 +233,9 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-                for (int kb = 0; kb < kb_total; ++kb) {
+                const int kb_lo = static_cast<int>(t / args.total_tiles) * args.kb_per_split;
+                const int kb_hi = min(kb_total, kb_lo + args.kb_per_split);
+                for (int kb = kb_lo; kb < kb_hi; ++kb) {
                     if (!mbar_wait_bounded(smem_u32(&full[s]), ph, abort_flag, args.status, tmo)) {
                         ok = false;
                         break;
@@ -248,7 +257,8 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                         } else {
                             bdesc = smem_desc_sw128(sb + kk * 32, 16, 1024);
                         }
-                        tc_mma_f16(d_tmem, adesc, bdesc, args.idesc, (kb | kk) != 0 ? 1u : 0u);
+                        tc_mma_f16(d_tmem, adesc, bdesc, args.idesc,
+                                   ((kb - kb_lo) | kk) != 0 ? 1u : 0u);
                     }
                     issued_any = true;
                     tc_commit(smem_u32(&empty[s]));  // stage s is free once these MMAs finish
@@ -281,13 +291,16 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
         int nchunk = 0;    // chunks this warp has staged (selects the buffer)
         bool ok = true;
         int lt = 0;
-        for (int64_t t = blockIdx.x; ok && t < args.total_tiles; t += gridDim.x, ++lt) {
+        for (int64_t t = blockIdx.x; ok && t < args.total_items; t += gridDim.x, ++lt) {
             const int buf = lt & 1;
             const uint32_t tph = static_cast<uint32_t>(lt >> 1) & 1u;
             if (!mbar_wait_bounded(smem_u32(&tfull[buf]), tph, abort_flag, args.status, tmo)) break;
             tc_fence_after();
-            int64_t b, mt, nt;
-            tc_tile_coords(t, args, b, mt, nt);
+            const int split = static_cast<int>(t / args.total_tiles);
+            int64_t bt, mt, nt;
+            tc_tile_coords(t - split * args.total_tiles, args, bt, mt, nt);
+            // output batch index: the partial-sum slab (batch, split) under split-K
+            const int64_t b = args.splits > 1 ? bt * args.splits + split : bt;
             const int32_t row0 = static_cast<int32_t>(mt * TBM + q * 32);
             const int64_t row = row0 + lane;
             const int64_t col0 = nt * BN;
@@ -320,7 +333,7 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                         mbar_arrive_expect_tx(smem_u32(&rb[sel]), EPI_BUF_BYTES);
                         tma_load_3d(smem_u32(sb), &tmR, smem_u32(&rb[sel]),
                                     static_cast<int32_t>(cg), row0,
-                                    static_cast<int32_t>(b * args.r_bmul));
+                                    static_cast<int32_t>(bt * args.r_bmul));
                     }
                     float y[64];
 #pragma unroll
@@ -374,7 +387,7 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                                 y[4 * j + 3] += e.beta * r4.w;
                             }
                         } else if (row < e.M) {
-                            const float* rp = e.R + b * e.stride_r + row * e.ldr + cg;
+                            const float* rp = e.R + bt * e.stride_r + row * e.ldr + cg;
 #pragma unroll
                             for (int i = 0; i < 64; ++i)
                                 if (i < W && cg + i < e.N) y[i] += e.beta * __ldg(rp + i);
@@ -408,7 +421,7 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                     __syncwarp();
                     if (lane == 0 && cg < args.n_tma) {
                         tma_store_3d(&tmC, smem_u32(sb), static_cast<int32_t>(cg), row0,
-                                     static_cast<int32_t>(b * args.c_bmul));
+                                     static_cast<int32_t>(bt * args.c_bmul + split * args.c_smul));
                         bulk_commit();
                     }
                     if (cg + W > args.n_tma && row < e.M) {
@@ -475,7 +488,7 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
 template <int BN, int STAGES, bool B_KN, int EW>
 cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& tmA,
                         const CUtensorMap& tmB, const TcEpiMaps* em, const Shape& s,
-                        const EpiParams& e, const LaunchCtx& lc) {
+                        const EpiParams& e, const LaunchCtx& lc, const EpiParams* final_epi) {
     TcArgs a{};
     a.M = s.M;
     a.N = s.N;
@@ -488,6 +501,7 @@ cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& 
     a.r_tma = em != nullptr && em->r_tma;
     a.out16 = e.out_dtype != GEMM_F32;
     a.c_bmul = em ? em->c_bmul : 0;
+    a.c_smul = em ? em->c_smul : 0;
     a.r_bmul = em ? em->r_bmul : 0;
     a.bias_vec = e.bias && (reinterpret_cast<uintptr_t>(e.bias) % 16 == 0);
     a.n_tma = em ? em->n_tma : 0;
@@ -496,6 +510,9 @@ cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& 
     a.tiles_per_batch = a.m_tiles * a.n_tiles;
     a.total_tiles = a.tiles_per_batch * s.batch;
     a.k_blocks = static_cast<int>((s.K + TBK - 1) / TBK);
+    a.splits = tc_effective_splits(s.K, cfg.split_k);
+    a.kb_per_split = (a.k_blocks + a.splits - 1) / a.splits;
+    a.total_items = a.total_tiles * a.splits;
     a.raster = cfg.raster_group > 0 ? cfg.raster_group : 16;
     // Instruction descriptor, kind::f16: D = F32 (bits 4-5 = 1); A and B type
     // (bits 7-9, 10-12) 0 = F16, 1 = BF16; A K-major (bit 15 = 0); B K-major
@@ -512,11 +529,15 @@ cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& 
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     int64_t grid = cfg.num_ctas > 0 ? cfg.num_ctas : lc.num_sms;
-    if (grid > a.total_tiles) grid = a.total_tiles;
+    if (grid > a.total_items) grid = a.total_items;
     if (grid < 1) grid = 1;
     kern<<<static_cast<unsigned>(grid), tc_threads<EW>(), smem, lc.stream>>>(
         tmA, tmB, em ? em->c : unused_map, (em && em->r_tma) ? em->r : unused_map, a);
-    return cudaGetLastError();
+    cudaError_t err2 = cudaGetLastError();
+    if (err2 != cudaSuccess || a.splits == 1) return err2;
+    // split-K: add the partial slabs in split order and apply the real epilogue
+    return launch_split_reduce(static_cast<const float*>(e.C), s.M, s.N, s.batch, a.splits,
+                               *final_epi, lc);
 }
 
 // Instantiated configurations: (BN, STAGES, epilogue warps).  Eight epilogue
@@ -532,10 +553,10 @@ cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& 
 template <bool B_KN>
 cudaError_t launch_tc_layout(const gemm_config_t& cfg, int dtype, const CUtensorMap& tmA,
                              const CUtensorMap& tmB, const TcEpiMaps* em, const Shape& s,
-                             const EpiParams& e, const LaunchCtx& lc) {
+                             const EpiParams& e, const LaunchCtx& lc, const EpiParams* fe) {
 #define G13_TC_LAUNCH(BN, ST, EW, VAR)                                                   \
     if (cfg.bn == BN && cfg.stages == ST && cfg.variant == VAR)                          \
-        return launch_tc_t<BN, ST, B_KN, EW>(cfg, dtype, tmA, tmB, em, s, e, lc);
+        return launch_tc_t<BN, ST, B_KN, EW>(cfg, dtype, tmA, tmB, em, s, e, lc, fe);
     G13_TC_CONFIGS(G13_TC_LAUNCH)
 #undef G13_TC_LAUNCH
     return cudaErrorInvalidValue;
@@ -552,11 +573,20 @@ size_t tc_smem_bytes(const gemm_config_t& cfg) {
     return 0;
 }
 
+int tc_effective_splits(int64_t K, int split_k) {
+    const int64_t kb = (K + TBK - 1) / TBK;
+    if (split_k <= 1 || kb <= 1) return 1;
+    const int64_t per = (kb + split_k - 1) / split_k;
+    return static_cast<int>((kb + per - 1) / per);
+}
+
 cudaError_t launch_tc(const gemm_config_t& cfg, int dtype, int b_layout, const CUtensorMap& tmA,
                       const CUtensorMap& tmB, const TcEpiMaps* em, const Shape& s,
-                      const EpiParams& e, const LaunchCtx& lc) {
-    if (b_layout == GEMM_B_KN) return launch_tc_layout<true>(cfg, dtype, tmA, tmB, em, s, e, lc);
-    return launch_tc_layout<false>(cfg, dtype, tmA, tmB, em, s, e, lc);
+                      const EpiParams& e, const LaunchCtx& lc, const EpiParams* final_epi) {
+    if (tc_effective_splits(s.K, cfg.split_k) > 1 && !final_epi) return cudaErrorInvalidValue;
+    if (b_layout == GEMM_B_KN)
+        return launch_tc_layout<true>(cfg, dtype, tmA, tmB, em, s, e, lc, final_epi);
+    return launch_tc_layout<false>(cfg, dtype, tmA, tmB, em, s, e, lc, final_epi);
 }
 
 #undef G13_TC_CONFIGS

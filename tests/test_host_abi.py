@@ -124,6 +124,8 @@ def test_dispatch_buckets(lib):
         assert sel("bf16", M, N, 1000).kernel == "skinny", (M, N)
     assert sel("bf16", 512, 512, 0).kernel == "skinny"      # K = 0: epilogue only
     assert sel("f32", 1, 4096, 4096).kernel == "skinny"
+    assert sel("bf16", 4, 4096, 4096).kernel == "skinny"
+    assert sel("bf16", 5, 4096, 4096).kernel == "tc"       # tensor cores (+ split-K) from 5 rows
 
 
 def test_dispatch_staging_follows_alignment(lib):
