@@ -44,7 +44,6 @@ struct FLayout {
     static constexpr int B_BYTES = FBK * BN * 4;  // 16 or 32 KB
     static constexpr int STAGE_BYTES = F_A_BYTES + B_BYTES;
     static constexpr int NQ = BN / 64;            // column quads per thread
-    static constexpr int CTAS_PER_SM = BN == 128 ? 2 : 1;
 };
 
 struct FfmaArgs {
@@ -122,8 +121,10 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, uint64
         if (globaltimer_ns() - t0 > timeout_ns) return;
 }
 
+// BN = 128 with row-major B runs two CTAs per SM (128 registers); the K-major
+// loop keeps more fragments live and runs one CTA per SM without spilling.
 template <int BN, int STAGES, bool B_NK, bool PACKED>
-__global__ void __launch_bounds__(FTHREADS, FLayout<BN>::CTAS_PER_SM)
+__global__ void __launch_bounds__(FTHREADS, (BN == 128 && !B_NK) ? 2 : 1)
     ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const FfmaArgs args) {
     using L = FLayout<BN>;
