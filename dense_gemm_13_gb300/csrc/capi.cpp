@@ -421,8 +421,9 @@ int gemm_run(gemm_plan_t plan, const void* A, const void* B, void* C, const void
                 rc = encode(&plan->mapA, p.dtype, a_src, ga.cols, ga.rows, lda, ga.batches, sa, 64,
                             128, CU_TENSOR_MAP_SWIZZLE_128B);
                 if (rc == GEMM_OK)
+                    // K-major B boxes hold the tile's columns (half of them per CTA of a pair)
                     rc = encode(&plan->mapB, p.dtype, b_src, gb.cols, gb.rows, ldb, gb.batches, sb,
-                                64, kn ? 64 : static_cast<uint32_t>(cfg.bn),
+                                64, kn ? 64 : static_cast<uint32_t>(tc_b_box_rows(cfg)),
                                 CU_TENSOR_MAP_SWIZZLE_128B);
             } else {
                 rc = encode(&plan->mapA, p.dtype, a_src, ga.cols, ga.rows, lda, ga.batches, sa, 32,

@@ -227,6 +227,23 @@ int choose_config(const Problem& p, int num_sms, gemm_config_t* out) {
         }
         c.raster_group = static_cast<int32_t>(std::min<int64_t>(16, mt));
         c.split_k = tc_splits(p, num_sms, c.bn);
+        // CTA pairs (cta_group::2, 256 x 256 tiles, 6 stages) move a third less
+        // operand data per SM for the same MMA work: 1876 vs 1602 TFLOPS at
+        // 8192^3 and 1521 vs 1242 at 4096^3 on GB300.  A pair tile costs one SM
+        // wave like a 128 x 256 tile but runs ~15 % faster; with short K the
+        // 8-warp epilogue of the single-CTA kernel wins instead.
+        if (c.split_k == 1 && K > 1024 && num_sms >= 2) {
+            const int64_t pair_waves = cdiv(bt * cdiv(M, 256) * cdiv(N, 256), num_sms / 2);
+            const int64_t cost_single =
+                (c.bn == 128 ? waves128 * 128 * 5 : waves256 * 256 * 4) * 100;
+            const int64_t cost_pair = pair_waves * 256 * 4 * 85;
+            if (cost_pair < cost_single) {
+                c.bn = 256;
+                c.stages = 6;
+                c.variant = TC_VARIANT_PAIR;
+                c.raster_group = static_cast<int32_t>(std::min<int64_t>(16, cdiv(M, 256)));
+            }
+        }
     }
     set_staging(p, &c);
     *out = c;
@@ -258,12 +275,15 @@ int check_config(const Problem& p, const gemm_config_t& in, gemm_config_t* out) 
             if (p.dtype == GEMM_F32 || p.K == 0) return GEMM_ERR_UNSUPPORTED;
             if (c.stream_k != 0) return GEMM_ERR_UNSUPPORTED;
             if (c.bm != 128 || c.bk != 64) return GEMM_ERR_UNSUPPORTED;
-            // (BN, stages) pairs with 4 epilogue warps (variant 0) or 8 (variant 1)
+            // (BN, stages) pairs with 4 epilogue warps (variant 0) or 8 (variant 1);
+            // variant 2: CTA pairs on 256 x 256 tiles, no split-K
             if (!((c.variant == 0 && ((c.bn == 256 && (c.stages == 4 || c.stages == 3)) ||
                                       (c.bn == 128 && (c.stages == 6 || c.stages == 4)))) ||
                   (c.variant == 1 && ((c.bn == 256 && c.stages == 3) ||
-                                      (c.bn == 128 && c.stages == 4)))))
+                                      (c.bn == 128 && c.stages == 4))) ||
+                  (c.variant == 2 && c.bn == 256 && (c.stages == 6 || c.stages == 4))))
                 return GEMM_ERR_UNSUPPORTED;
+            if (c.variant == 2 && c.split_k > 1) return GEMM_ERR_UNSUPPORTED;
             if (c.raster_group == 0) c.raster_group = 16;
             break;
         default:

@@ -68,6 +68,12 @@ cudaError_t launch_split_reduce(const float* partial, int64_t M, int64_t N, int6
                                 int splits, const EpiParams& e, const LaunchCtx& lc);
 // Shared memory the TC kernel needs for a config (bytes), or 0 if unsupported.
 size_t tc_smem_bytes(const gemm_config_t& cfg);
+// TC config variant that runs CTA pairs (tcgen05 cta_group::2, 256-row tiles).
+constexpr int TC_VARIANT_PAIR = 2;
+// Rows of a K-major B box: the tile's columns, split between the CTAs of a pair.
+inline int tc_b_box_rows(const gemm_config_t& cfg) {
+    return cfg.variant == TC_VARIANT_PAIR ? cfg.bn / 2 : cfg.bn;
+}
 
 // FP32 FFMA path: A via tmA (dims K, M, batch), B via tmB (KN: N, K, batch; NK: K, N, batch).
 cudaError_t launch_ffma(const gemm_config_t& cfg, int b_layout, const CUtensorMap& tmA,

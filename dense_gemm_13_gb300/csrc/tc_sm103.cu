@@ -23,7 +23,17 @@
 //               Layouts TMA cannot address fall back to per-thread stores.
 //
 // The grid is persistent (one CTA per SM); CTA c walks tiles c, c+grid, ...
-// in a grouped raster order.  The double-buffered accumulator lets the
+// in a grouped raster order.
+//
+// Pair mode (PAIR): clusters of two CTAs on two SMs share one 256 x BN tile
+// through tcgen05 cta_group::2.  Each CTA loads its own 128 rows of A and its
+// own BN/2 columns of B, so a CTA moves 32 KB per 64-deep K block instead of
+// 48 KB for a 128 x 256 tile; the even CTA's MMA thread issues 256 x BN x 16
+// MMAs that read both CTAs' shared memory and write each CTA's 128 rows of the
+// accumulator into that CTA's TMEM.  Both CTAs' TMA loads for a stage count
+// their bytes on the even CTA's full[s] barrier (cta_group::2 TMA), the even
+// CTA's commits are multicast to both CTAs' stage and accumulator barriers,
+// and both CTAs' epilogue warps return accumulator buffers to the even CTA.  The double-buffered accumulator lets the
 // epilogue of tile t overlap the main loop of tile t+1.  Out-of-range rows,
 // columns and K arrive from TMA as zeros, so the main loop has no edge code.
 //
@@ -33,6 +43,8 @@
 //
 // Every wait is bounded (ptx.cuh); on a timeout the CTA drains its own copies
 // and MMAs, frees TMEM and exits, and the plan's status word records it.
+#include <atomic>
+
 #include "epilogue.cuh"
 #include "internal.h"
 #include "ptx.cuh"
@@ -40,14 +52,18 @@
 namespace g13 {
 namespace {
 
+constexpr int kMaxDevices = 64;
+
 constexpr int TBM = 128, TBK = 64;
 constexpr int T_A_BYTES = TBM * TBK * 2;  // 16 KB: 128 rows x 128 B
 constexpr int EPI_BUF_BYTES = 32 * 128;   // one 32-row x 128-byte output (or residual) chunk
 
-template <int BN>
+template <int BN, bool PAIR>
 struct TcLayout {
-    static constexpr int B_BYTES = BN * TBK * 2;  // BN x 128 B
+    static constexpr int B_ROWS = PAIR ? BN / 2 : BN;   // B columns this CTA loads
+    static constexpr int B_BYTES = B_ROWS * TBK * 2;    // B_ROWS x 128 B
     static constexpr int STAGE_BYTES = T_A_BYTES + B_BYTES;
+    static constexpr int TILE_M = PAIR ? 2 * TBM : TBM; // rows of a (pair) tile
 };
 
 struct TcArgs {
@@ -80,19 +96,19 @@ template <int EW>
 __host__ __device__ constexpr int tc_threads() {
     return 64 + 32 * EW;
 }
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool PAIR>
 __host__ __device__ constexpr int tc_epi_off() {
-    return STAGES * TcLayout<BN>::STAGE_BYTES;
+    return STAGES * TcLayout<BN, PAIR>::STAGE_BYTES;
 }
-template <int BN, int STAGES, int EW>
+template <int BN, int STAGES, int EW, bool PAIR>
 __host__ __device__ constexpr int tc_bar_off() {
-    return tc_epi_off<BN, STAGES>() + EW * 2 * EPI_BUF_BYTES;
+    return tc_epi_off<BN, STAGES, PAIR>() + EW * 2 * EPI_BUF_BYTES;
 }
-template <int BN, int STAGES, int EW>
+template <int BN, int STAGES, int EW, bool PAIR>
 __host__ __device__ constexpr int tc_smem_total() {
     // ring + epilogue tiles + full/empty per stage + tfull/tempty x2 + drain
     // + residual barriers (2 per epilogue warp) + tmem slot + abort flag
-    return 1024 + tc_bar_off<BN, STAGES, EW>() + (2 * STAGES + 5 + 2 * EW) * 8 + 16;
+    return 1024 + tc_bar_off<BN, STAGES, EW, PAIR>() + (2 * STAGES + 5 + 2 * EW) * 8 + 16;
 }
 
 __device__ __forceinline__ void tc_tile_coords(int64_t t, const TcArgs& a, int64_t& b, int64_t& mt,
@@ -114,17 +130,17 @@ __device__ __forceinline__ void tc_drain(uint32_t bar, uint32_t parity, uint64_t
         if (globaltimer_ns() - t0 > timeout_ns) return;
 }
 
-template <int BN, int STAGES, bool B_KN, int EW>
+template <int BN, int STAGES, bool B_KN, int EW, bool PAIR>
 __global__ void __launch_bounds__(tc_threads<EW>(), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmR,
                    const TcArgs args) {
-    using L = TcLayout<BN>;
+    using L = TcLayout<BN, PAIR>;
     constexpr uint32_t TMEM_COLS = 2 * BN;  // 256 or 512: powers of two
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + tc_bar_off<BN, STAGES, EW>());
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + tc_bar_off<BN, STAGES, EW, PAIR>());
     uint64_t* empty = full + STAGES;
     uint64_t* tfull = empty + STAGES;
     uint64_t* tempty = tfull + 2;
@@ -134,6 +150,10 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Pair mode: rank 0 / 1 in the CTA pair; the pair walks tiles together.
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const int64_t first_item = PAIR ? (blockIdx.x >> 1) : blockIdx.x;
+    const int64_t item_stride = PAIR ? (gridDim.x >> 1) : gridDim.x;
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -142,7 +162,8 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&tfull[i]), 1);
-            mbar_init(smem_u32(&tempty[i]), 32 * EW);
+            // pair mode: lane 0 of every epilogue warp of both CTAs; else every epilogue thread
+            mbar_init(smem_u32(&tempty[i]), PAIR ? 2 * EW : 32 * EW);
         }
         mbar_init(smem_u32(drain), 1);
         for (int i = 0; i < 2 * EW; ++i) mbar_init(smem_u32(&rbar[i]), 1);
@@ -151,9 +172,15 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }
-    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    if (warp == 1) {
+        if (PAIR)
+            tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+        else
+            tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    }
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();  // the peer's barriers are initialised before any remote arrive
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -168,12 +195,13 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
             uint32_t ph = 0;
             uint32_t armed = 0, armed_par = 0;  // per stage: armed and not yet seen consumed
             bool ok = true;
-            for (int64_t t = blockIdx.x; ok && t < args.total_items; t += gridDim.x) {
+            for (int64_t t = first_item; ok && t < args.total_items; t += item_stride) {
                 const int split = static_cast<int>(t / args.total_tiles);
                 int64_t b, mt, nt;
                 tc_tile_coords(t - split * args.total_tiles, args, b, mt, nt);
-                const int32_t m0 = static_cast<int32_t>(mt * TBM);
-                const int32_t n0 = static_cast<int32_t>(nt * BN);
+                // this CTA's rows of A and columns of B
+                const int32_t m0 = static_cast<int32_t>(mt * L::TILE_M + rank * TBM);
+                const int32_t n0 = static_cast<int32_t>(nt * BN + rank * L::B_ROWS);
                 const int kb_lo = split * args.kb_per_split;
                 const int kb_hi = min(kb_total, kb_lo + args.kb_per_split);
                 for (int kb = kb_lo; kb < kb_hi; ++kb) {
@@ -183,22 +211,33 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                         break;
                     }
                     armed &= ~(1u << s);  // the previous use of this stage was consumed
-                    const bool skip = stall && t == blockIdx.x && kb == kb_lo;
+                    const bool skip = stall && t == first_item && kb == kb_lo;
                     if (!skip) {
-                        const uint32_t bar = smem_u32(&full[s]);
                         uint8_t* sa = smem + s * L::STAGE_BYTES;
                         uint8_t* sb = sa + T_A_BYTES;
-                        mbar_arrive_expect_tx(bar, L::STAGE_BYTES);
                         const int32_t ba = static_cast<int32_t>(b * args.a_bmul);
                         const int32_t bb = static_cast<int32_t>(b * args.b_bmul);
-                        tma_load_3d(smem_u32(sa), &tmA, bar, kb * TBK, m0, ba);
+                        // In a pair, both CTAs' boxes for stage s land on the even
+                        // CTA's full[s], which expects both CTAs' bytes.
+                        const uint32_t bar =
+                            PAIR ? mapa_shared(smem_u32(&full[s]), 0) : smem_u32(&full[s]);
+                        if (rank == 0)
+                            mbar_arrive_expect_tx(smem_u32(&full[s]),
+                                                  (PAIR ? 2 : 1) * L::STAGE_BYTES);
+                        const auto load = [&](uint32_t dst, const CUtensorMap* m, int32_t c0,
+                                              int32_t c1, int32_t c2) {
+                            if (PAIR)
+                                tma_load_3d_pair(dst, m, bar, c0, c1, c2);
+                            else
+                                tma_load_3d(dst, m, bar, c0, c1, c2);
+                        };
+                        load(smem_u32(sa), &tmA, kb * TBK, m0, ba);
                         if (B_KN) {
 #pragma unroll
-                            for (int j = 0; j < BN / 64; ++j)
-                                tma_load_3d(smem_u32(sb + j * (64 * 128)), &tmB, bar, n0 + 64 * j,
-                                            kb * TBK, bb);
+                            for (int j = 0; j < L::B_ROWS / 64; ++j)
+                                load(smem_u32(sb + j * (64 * 128)), &tmB, n0 + 64 * j, kb * TBK, bb);
                         } else {
-                            tma_load_3d(smem_u32(sb), &tmB, bar, kb * TBK, n0, bb);
+                            load(smem_u32(sb), &tmB, kb * TBK, n0, bb);
                         }
                         armed |= 1u << s;
                         armed_par = (armed_par & ~(1u << s)) | (ph << s);
@@ -211,19 +250,32 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
             }
             if (!ok) {
                 // Let our own copies land before the CTA's shared memory goes away.
-                for (int i = 0; i < STAGES; ++i)
-                    if (armed & (1u << i)) tc_drain(smem_u32(&full[i]), (armed_par >> i) & 1u, tmo);
+                if (PAIR && rank == 1) {
+                    // they count on the even CTA's barriers, which this CTA cannot
+                    // wait on: give them a fixed 200 us (a copy takes a few us)
+                    if (armed) {
+                        const uint64_t t0 = globaltimer_ns();
+                        while (globaltimer_ns() - t0 < 200000ull) {
+                        }
+                    }
+                } else {
+                    for (int i = 0; i < STAGES; ++i)
+                        if (armed & (1u << i))
+                            tc_drain(smem_u32(&full[i]), (armed_par >> i) & 1u, tmo);
+                }
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && rank == 0) {
             // ------------------------------------------------ MMA issuer
+            // (in a pair, only the even CTA's thread issues; the odd CTA's
+            // warp 1 only holds its half of the TMEM allocation)
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
             bool issued_any = false;
             int lt = 0;
-            for (int64_t t = blockIdx.x; ok && t < args.total_items; t += gridDim.x, ++lt) {
+            for (int64_t t = first_item; ok && t < args.total_items; t += item_stride, ++lt) {
                 const int buf = lt & 1;
                 const uint32_t tph = static_cast<uint32_t>(lt >> 1) & 1u;
                 if (!mbar_wait_bounded(smem_u32(&tempty[buf]), tph ^ 1u, abort_flag, args.status,
@@ -257,22 +309,36 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                         } else {
                             bdesc = smem_desc_sw128(sb + kk * 32, 16, 1024);
                         }
-                        tc_mma_f16(d_tmem, adesc, bdesc, args.idesc,
-                                   ((kb - kb_lo) | kk) != 0 ? 1u : 0u);
+                        const uint32_t acc = ((kb - kb_lo) | kk) != 0 ? 1u : 0u;
+                        if (PAIR)
+                            tc_mma_f16_pair(d_tmem, adesc, bdesc, args.idesc, acc);
+                        else
+                            tc_mma_f16(d_tmem, adesc, bdesc, args.idesc, acc);
                     }
                     issued_any = true;
-                    tc_commit(smem_u32(&empty[s]));  // stage s is free once these MMAs finish
+                    // stage s (in both CTAs of a pair) is free once these MMAs finish
+                    if (PAIR)
+                        tc_commit_pair(smem_u32(&empty[s]), 0x3);
+                    else
+                        tc_commit(smem_u32(&empty[s]));
                     if (++s == STAGES) {
                         s = 0;
                         ph ^= 1u;
                     }
                 }
                 if (!ok) break;
-                tc_commit(smem_u32(&tfull[buf]));  // accumulator ready for the epilogue
+                // accumulator ready for the epilogue (of both CTAs of a pair)
+                if (PAIR)
+                    tc_commit_pair(smem_u32(&tfull[buf]), 0x3);
+                else
+                    tc_commit(smem_u32(&tfull[buf]));
             }
             if (!ok && issued_any) {
                 // Wait for every MMA already issued before TMEM is released.
-                tc_commit(smem_u32(drain));
+                if (PAIR)
+                    tc_commit_pair(smem_u32(drain), 0x1);
+                else
+                    tc_commit(smem_u32(drain));
                 tc_drain(smem_u32(drain), 0u, tmo);
             }
         }
@@ -284,14 +350,24 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
         constexpr int SLICE = BN / (EW / 4);
         const int c_lo = (ew >> 2) * SLICE;
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-        uint8_t* etile = smem + tc_epi_off<BN, STAGES>() + ew * 2 * EPI_BUF_BYTES;
+        uint8_t* etile = smem + tc_epi_off<BN, STAGES, PAIR>() + ew * 2 * EPI_BUF_BYTES;
+        // Hand an accumulator buffer back to the MMA thread (the even CTA's in a pair).
+        const auto release = [&](int buf) {
+            tc_fence_before();
+            if (PAIR) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[buf]), 0));
+            } else {
+                mbar_arrive(smem_u32(&tempty[buf]));
+            }
+        };
         uint64_t* rb = rbar + 2 * ew;
         const EpiParams& e = args.e;
         uint32_t rph = 0;  // bit i: phase parity of rb[i]
         int nchunk = 0;    // chunks this warp has staged (selects the buffer)
         bool ok = true;
         int lt = 0;
-        for (int64_t t = blockIdx.x; ok && t < args.total_items; t += gridDim.x, ++lt) {
+        for (int64_t t = first_item; ok && t < args.total_items; t += item_stride, ++lt) {
             const int buf = lt & 1;
             const uint32_t tph = static_cast<uint32_t>(lt >> 1) & 1u;
             if (!mbar_wait_bounded(smem_u32(&tfull[buf]), tph, abort_flag, args.status, tmo)) break;
@@ -301,7 +377,7 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
             tc_tile_coords(t - split * args.total_tiles, args, bt, mt, nt);
             // output batch index: the partial-sum slab (batch, split) under split-K
             const int64_t b = args.splits > 1 ? bt * args.splits + split : bt;
-            const int32_t row0 = static_cast<int32_t>(mt * TBM + q * 32);
+            const int32_t row0 = static_cast<int32_t>(mt * L::TILE_M + rank * TBM + q * 32);
             const int64_t row = row0 + lane;
             const int64_t col0 = nt * BN;
             const uint32_t tbase = tmem_base + lane_base + static_cast<uint32_t>(buf * BN);
@@ -317,8 +393,7 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                     tmem_ld_wait();
                     if (c + W >= c_lo + SLICE) {
                         // This warp's part of the accumulator is in registers: release it.
-                        tc_fence_before();
-                        mbar_arrive(smem_u32(&tempty[buf]));
+                        release(buf);
                     }
                     const int64_t cg = col0 + c;  // first global column of the chunk
                     if (cg >= e.N) continue;
@@ -458,8 +533,7 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                     tmem_ld_wait();
                     if (c == (c_lo + SLICE) / 32 - 1) {
                         // All of this buffer is in registers: hand it back to the MMA warp.
-                        tc_fence_before();
-                        mbar_arrive(smem_u32(&tempty[buf]));
+                        release(buf);
                     }
                     if (col0 + c * 32 < e.N) {
 #pragma unroll
@@ -478,17 +552,23 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
 
     tc_fence_before();
     __syncthreads();
+    // A pair's CTAs stay resident until neither will touch the other's shared memory.
+    if (PAIR) cluster_sync();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        if (PAIR)
+            tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 
-template <int BN, int STAGES, bool B_KN, int EW>
+template <int BN, int STAGES, bool B_KN, int EW, bool PAIR>
 cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& tmA,
                         const CUtensorMap& tmB, const TcEpiMaps* em, const Shape& s,
                         const EpiParams& e, const LaunchCtx& lc, const EpiParams* final_epi) {
+    using L = TcLayout<BN, PAIR>;
     TcArgs a{};
     a.M = s.M;
     a.N = s.N;
@@ -505,12 +585,12 @@ cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& 
     a.r_bmul = em ? em->r_bmul : 0;
     a.bias_vec = e.bias && (reinterpret_cast<uintptr_t>(e.bias) % 16 == 0);
     a.n_tma = em ? em->n_tma : 0;
-    a.m_tiles = (s.M + TBM - 1) / TBM;
+    a.m_tiles = (s.M + L::TILE_M - 1) / L::TILE_M;
     a.n_tiles = (s.N + BN - 1) / BN;
     a.tiles_per_batch = a.m_tiles * a.n_tiles;
     a.total_tiles = a.tiles_per_batch * s.batch;
     a.k_blocks = static_cast<int>((s.K + TBK - 1) / TBK);
-    a.splits = tc_effective_splits(s.K, cfg.split_k);
+    a.splits = PAIR ? 1 : tc_effective_splits(s.K, cfg.split_k);
     a.kb_per_split = (a.k_blocks + a.splits - 1) / a.splits;
     a.total_items = a.total_tiles * a.splits;
     a.raster = cfg.raster_group > 0 ? cfg.raster_group : 16;
@@ -519,44 +599,84 @@ cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& 
     // (bit 16 = 0) or MN-major (1); N >> 3 at bits 17-22; M >> 4 at bits 24-28.
     const uint32_t ab = dtype == GEMM_BF16 ? 1u : 0u;
     a.idesc = (1u << 4) | (ab << 7) | (ab << 10) | ((B_KN ? 1u : 0u) << 16) |
-              (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(TBM >> 4) << 24);
+              (static_cast<uint32_t>(BN >> 3) << 17) |
+              (static_cast<uint32_t>(L::TILE_M >> 4) << 24);
     a.e = e;
     a.status = lc.status;
     a.timeout_ns = lc.timeout_ns;
     a.flags = lc.flags;
-    const int smem = tc_smem_total<BN, STAGES, EW>();
-    auto kern = tc_gemm_kernel<BN, STAGES, B_KN, EW>;
+    const int smem = tc_smem_total<BN, STAGES, EW, PAIR>();
+    auto kern = tc_gemm_kernel<BN, STAGES, B_KN, EW, PAIR>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
+    const CUtensorMap& mc = em ? em->c : unused_map;
+    const CUtensorMap& mr = (em && em->r_tma) ? em->r : unused_map;
+    cudaError_t err2;
+    if (PAIR) {
+        // clusters of two CTAs, as many pairs as can be resident at once
+        cudaLaunchConfig_t lcfg = {};
+        lcfg.blockDim = dim3(tc_threads<EW>());
+        lcfg.dynamicSmemBytes = smem;
+        lcfg.stream = lc.stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        lcfg.attrs = attr;
+        lcfg.numAttrs = 1;
+        int64_t pairs = cfg.num_ctas > 0 ? cfg.num_ctas / 2 : lc.num_sms / 2;
+        lcfg.gridDim = dim3(static_cast<unsigned>(2 * (pairs > 0 ? pairs : 1)));
+        // resident pairs per device, looked up once per instantiation and device
+        static std::atomic<int> resident[kMaxDevices];
+        int dev = 0;
+        err = cudaGetDevice(&dev);
+        if (err != cudaSuccess) return err;
+        int max_pairs = dev >= 0 && dev < kMaxDevices ? resident[dev].load() : 0;
+        if (max_pairs == 0) {
+            err = cudaOccupancyMaxActiveClusters(&max_pairs, kern, &lcfg);
+            if (err != cudaSuccess) return err;
+            if (dev >= 0 && dev < kMaxDevices) resident[dev].store(max_pairs);
+        }
+        if (max_pairs < 1) return cudaErrorInvalidConfiguration;
+        if (pairs > max_pairs) pairs = max_pairs;
+        if (pairs > a.total_items) pairs = a.total_items;
+        if (pairs < 1) pairs = 1;
+        lcfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+        err2 = cudaLaunchKernelEx(&lcfg, kern, tmA, tmB, mc, mr, a);
+        return err2;
+    }
     int64_t grid = cfg.num_ctas > 0 ? cfg.num_ctas : lc.num_sms;
     if (grid > a.total_items) grid = a.total_items;
     if (grid < 1) grid = 1;
-    kern<<<static_cast<unsigned>(grid), tc_threads<EW>(), smem, lc.stream>>>(
-        tmA, tmB, em ? em->c : unused_map, (em && em->r_tma) ? em->r : unused_map, a);
-    cudaError_t err2 = cudaGetLastError();
+    kern<<<static_cast<unsigned>(grid), tc_threads<EW>(), smem, lc.stream>>>(tmA, tmB, mc, mr, a);
+    err2 = cudaGetLastError();
     if (err2 != cudaSuccess || a.splits == 1) return err2;
     // split-K: add the partial slabs in split order and apply the real epilogue
     return launch_split_reduce(static_cast<const float*>(e.C), s.M, s.N, s.batch, a.splits,
                                *final_epi, lc);
 }
 
-// Instantiated configurations: (BN, STAGES, epilogue warps).  Eight epilogue
-// warps (variant 1) take 64 KB of staging tiles, so they pair with fewer stages.
-#define G13_TC_CONFIGS(X) \
-    X(256, 4, 4, 0)       \
-    X(256, 3, 4, 0)       \
-    X(128, 6, 4, 0)       \
-    X(128, 4, 4, 0)       \
-    X(256, 3, 8, 1)       \
-    X(128, 4, 8, 1)
+// Instantiated configurations: (BN, STAGES, epilogue warps, variant, pair).
+// Eight epilogue warps (variant 1) take 64 KB of staging tiles, so they pair
+// with fewer stages; variant 2 is the CTA-pair kernel (32 KB stages).
+#define G13_TC_CONFIGS(X)    \
+    X(256, 4, 4, 0, false)   \
+    X(256, 3, 4, 0, false)   \
+    X(128, 6, 4, 0, false)   \
+    X(128, 4, 4, 0, false)   \
+    X(256, 3, 8, 1, false)   \
+    X(128, 4, 8, 1, false)   \
+    X(256, 6, 4, 2, true)    \
+    X(256, 4, 4, 2, true)
 
 template <bool B_KN>
 cudaError_t launch_tc_layout(const gemm_config_t& cfg, int dtype, const CUtensorMap& tmA,
                              const CUtensorMap& tmB, const TcEpiMaps* em, const Shape& s,
                              const EpiParams& e, const LaunchCtx& lc, const EpiParams* fe) {
-#define G13_TC_LAUNCH(BN, ST, EW, VAR)                                                   \
+#define G13_TC_LAUNCH(BN, ST, EW, VAR, PAIR)                                             \
     if (cfg.bn == BN && cfg.stages == ST && cfg.variant == VAR)                          \
-        return launch_tc_t<BN, ST, B_KN, EW>(cfg, dtype, tmA, tmB, em, s, e, lc, fe);
+        return launch_tc_t<BN, ST, B_KN, EW, PAIR>(cfg, dtype, tmA, tmB, em, s, e, lc, fe);
     G13_TC_CONFIGS(G13_TC_LAUNCH)
 #undef G13_TC_LAUNCH
     return cudaErrorInvalidValue;
@@ -566,8 +686,9 @@ cudaError_t launch_tc_layout(const gemm_config_t& cfg, int dtype, const CUtensor
 
 size_t tc_smem_bytes(const gemm_config_t& cfg) {
     if (cfg.bm != TBM || cfg.bk != TBK) return 0;
-#define G13_TC_SMEM(BN, ST, EW, VAR) \
-    if (cfg.bn == BN && cfg.stages == ST && cfg.variant == VAR) return tc_smem_total<BN, ST, EW>();
+#define G13_TC_SMEM(BN, ST, EW, VAR, PAIR)                      \
+    if (cfg.bn == BN && cfg.stages == ST && cfg.variant == VAR) \
+        return tc_smem_total<BN, ST, EW, PAIR>();
     G13_TC_CONFIGS(G13_TC_SMEM)
 #undef G13_TC_SMEM
     return 0;

@@ -60,7 +60,10 @@ def test_exact_integer(dtype, layout, shape):
 TC_CONFIGS = [g13.Config("tc", 128, 256, 64, 4), g13.Config("tc", 128, 256, 64, 3),
               g13.Config("tc", 128, 128, 64, 6), g13.Config("tc", 128, 128, 64, 4),
               g13.Config("tc", 128, 256, 64, 3, variant=1),
-              g13.Config("tc", 128, 128, 64, 4, variant=1)]
+              g13.Config("tc", 128, 128, 64, 4, variant=1),
+              # CTA pairs (tcgen05 cta_group::2) on 256 x 256 tiles
+              g13.Config("tc", 128, 256, 64, 6, variant=2),
+              g13.Config("tc", 128, 256, 64, 4, variant=2)]
 
 
 @pytest.mark.parametrize("cfg", TC_CONFIGS, ids=lambda c: f"bn{c.bn}s{c.stages}v{c.variant}")
@@ -80,6 +83,17 @@ def test_tc_variants_exact(cfg, dtype, layout):
     run2 = Run(w, tensors=run.t, config=cfg2)
     C2 = run2.run().result()
     assert np.array_equal(C2, cref.reshape(C.shape)), f"{w.name} {cfg2} (2 CTAs)"
+
+
+def test_tc_pair_epilogue_batched():
+    # CTA-pair kernel: 3 x 3 pair tiles per batch with ragged edges, every
+    # epilogue step, BF16 output through the TMA store path and an odd ldc
+    for layout in ("kn", "nk"):
+        w = Workload(f"tc_pair_epi_{layout}", "bf16", 700, 520, 1000, batch=2, b_layout=layout,
+                     bias=True, act="gelu", residual=True, beta=0.5, alpha=0.25,
+                     out_dtype="bf16")
+        full_check(Run(w, config=g13.Config("tc", 128, 256, 64, 6, variant=2)))
+        full_check(Run(w, config=g13.Config("tc", 128, 256, 64, 4, variant=2), ldc_pad=1))
 
 
 @pytest.mark.parametrize("split", [2, 3, 7])

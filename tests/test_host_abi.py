@@ -115,11 +115,15 @@ def test_dispatch_buckets(lib):
     assert sel("f32", 4096, 4096, 4096, "nk").variant == 0
     assert sel("f32", 256, 256, 256).kernel == "ffma"
     c = sel("bf16", 8192, 8192, 8192, "nk")
-    assert (c.kernel, c.bm, c.bn, c.bk) == ("tc", 128, 256, 64)
+    assert (c.kernel, c.bm, c.bn, c.bk, c.variant, c.stages) == ("tc", 128, 256, 64, 2, 6)  # pairs
     c = sel("f16", 4096, 3072, 768, "nk")
     assert (c.kernel, c.variant, c.stages) == ("tc", 1, 3)   # short K: 8 epilogue warps
     c = sel("bf16", 4096, 768, 3072, "kn")
-    assert (c.kernel, c.variant) == ("tc", 0)
+    assert (c.kernel, c.variant) == ("tc", 2)                # 48 pair tiles: one wave of pairs
+    c = sel("bf16", 256, 256, 4096, "nk")
+    assert (c.kernel, c.variant) == ("tc", 0) and c.split_k > 1   # split-K runs single CTAs
+    c = sel("bf16", 8192, 8192, 8192, "nk", sms=1)
+    assert c.variant != 2                                    # a pair needs two SMs
     for M, N in ((1, 6144), (6144, 1), (0, 10), (10, 0)):
         assert sel("bf16", M, N, 1000).kernel == "skinny", (M, N)
     assert sel("bf16", 512, 512, 0).kernel == "skinny"      # K = 0: epilogue only
