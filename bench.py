@@ -35,6 +35,7 @@ sys.path.insert(0, ROOT)
 
 FP32_LANES_PER_SM = 128          # FP32 FMA lanes per SM (4 partitions x 32)
 L2_FLUSH_BYTES = 512 << 20       # > 129 MB L2
+TF32_PER_BF16 = 1.1 / 2.25         # nominal dense TF32 / BF16 tensor rates
 
 
 def parse():
@@ -182,12 +183,13 @@ def make_device_inputs(w, seed, device):
     return t, dev
 
 
-def make_plan(g13, w):
+def make_plan(g13, w, flags=0):
     bt = w.batch
     ep = g13.Epilogue(b_layout=w.b_layout, out_dtype=w.out_dtype, bias=w.bias, act=w.act,
                       residual=w.residual, beta=w.beta, batch=bt,
                       stride_a=w.M * w.K if bt > 1 else 0, stride_b=w.N * w.K if bt > 1 else 0,
-                      stride_c=w.M * w.N if bt > 1 else 0, stride_r=w.M * w.N if (bt > 1 and w.residual) else 0)
+                      stride_c=w.M * w.N if bt > 1 else 0, stride_r=w.M * w.N if (bt > 1 and w.residual) else 0,
+                      flags=flags)
     ldb = w.N if w.b_layout == "kn" else w.K
     return g13.gemm_plan(w.dtype, w.M, w.N, w.K, w.K, ldb, w.N, ep)
 
@@ -271,6 +273,13 @@ def roofline_for(w, kernel, ms, pk, pk_kind):
         return {"bound": "alu", "achieved": flops / (ms * 1e-3) / 1e12, "peak": round(peak, 2),
                 "unit": "TFLOP/s", "peak_source": f"derived: {sm_count} SMs x {FP32_LANES_PER_SM} FP32 "
                 f"FMA lanes x 2 x {pk.get('sm_max_mhz', 2070.0):.0f} MHz"}
+    if kernel == "tf32x3":
+        # three TF32 MMAs per product on the tensor cores; TF32 runs at the nominal
+        # 1.1 / 2.25 of the BF16 rate, applied to the measured BF16 peak
+        peak = pk["bf16_tflops"] * TF32_PER_BF16
+        return {"bound": "tensor", "achieved": 3 * flops / (ms * 1e-3) / 1e12,
+                "peak": round(peak, 1), "unit": "TFLOP/s (TF32 MMA work, 3 x 2MNK)",
+                "peak_source": f"{pk_kind} bf16_tflops x {TF32_PER_BF16:.3f} (nominal TF32/BF16)"}
     byts = w.algorithmic_bytes()
     ai = flops / byts
     bw = pk["hbm_gbs"] * 1e9
@@ -285,7 +294,7 @@ def roofline_for(w, kernel, ms, pk, pk_kind):
 def sweep_summary(g13, torch, device, pk, pk_kind, reps=8):
     """Times all 343 ragged sweep triples (BF16, C = 0.5 AB + R) and summarises per bucket.
 
-    Buckets by the dispatcher's kernel and regime: skinny (M or N <= 16), tensor-core
+    Buckets by the dispatcher's kernel and regime: skinny (M or N <= 4), tensor-core
     problems that are HBM-bound by their arithmetic intensity, and compute-bound ones.
     Each triple: 2 warm-up runs, then `reps` runs each between an L2 flush and a CUDA
     event pair; median time.  Roofline fraction as in the main line.
@@ -436,12 +445,13 @@ def run_ours(args):
     if not args.no_extra:
         extra = []
         for name in ("bf16_8192", "bf16_4096", "ffn1_bf16", "ffn1_f16", "ffn2_bf16", "qkt_bf16",
-                     "sgemm_256"):
+                     "sgemm_256", "sgemm_4096+3xtf32"):
             if name == w.name:
                 continue
-            wx = WORKLOADS[name]
+            base, _, mode = name.partition("+")
+            wx = WORKLOADS[base]
             hx, dx = make_device_inputs(wx, 0, device)
-            px = make_plan(g13, wx)
+            px = make_plan(g13, wx, g13.FLAG_FP32_TENSOR if mode == "3xtf32" else 0)
             ox = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[wx.out_dtype]
             Cx = torch.empty((wx.M, wx.N) if wx.batch == 1 else (wx.batch, wx.M, wx.N), dtype=ox,
                              device=device)

@@ -25,8 +25,9 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgemm13.s
 DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
 ACTS = {"none": 0, "gelu": 1, "relu": 2}
 LAYOUTS = {"kn": 0, "nk": 1}
-KERNELS = {"auto": 0, "tc": 1, "ffma": 2, "skinny": 3}
+KERNELS = {"auto": 0, "tc": 1, "ffma": 2, "skinny": 3, "tf32x3": 4}
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
+FLAG_FP32_TENSOR = 0x1         # FP32 inputs may run as 3xTF32 on the tensor cores
 FLAG_TEST_STALL = 0x80000000
 
 STATUS = {0: "GEMM_OK", -1: "GEMM_ERR_INVALID_ARG", -2: "GEMM_ERR_UNSUPPORTED",

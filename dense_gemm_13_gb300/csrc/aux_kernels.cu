@@ -514,6 +514,112 @@ cudaError_t launch_skinny(const gemm_config_t& cfg, const SkinnyArgs& a, const S
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------ 3xTF32 split
+// x = hi + lo with hi = x rounded to TF32 (10 explicit mantissa bits, nearest,
+// ties away) and lo = x - hi, which is exact in FP32 (x and hi are within half
+// a TF32 ulp).  The tensor core reads lo as TF32 too, so A.B ~ Ah.Bh + Ah.Bl +
+// Al.Bh keeps about 21 bits of each operand.
+__device__ __forceinline__ void tf32_split(float x, float& hi, float& lo) {
+    uint32_t u;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(u) : "f"(x));
+    float h = __uint_as_float(u);
+    if (isinf(h) && !isinf(x)) h = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);  // no overflow
+    hi = h;
+    lo = isfinite(x) ? x - h : 0.0f;
+}
+
+// out[b][0 / 1][r][c] = hi / lo of X[b][r][c]; columns cols .. ldo-1 are zero.
+__global__ void __launch_bounds__(256) tf32_split_rows_kernel(const float* __restrict__ X,
+                                                              int64_t rows, int64_t cols,
+                                                              int64_t ld, int64_t bstride,
+                                                              int64_t batches, int vec,
+                                                              float* __restrict__ out,
+                                                              int64_t ldo) {
+    const int64_t q = ldo / 4;  // 4-column groups per output row
+    const int64_t total = batches * rows * q;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t g = i % q, br = i / q;
+        const int64_t r = br % rows, b = br / rows;
+        const int64_t c0 = 4 * g;
+        const float* src = X + b * bstride + r * ld + c0;
+        float v[4];
+        if (vec && c0 + 4 <= cols) {
+            const float4 t = __ldg(reinterpret_cast<const float4*>(src));
+            v[0] = t.x;
+            v[1] = t.y;
+            v[2] = t.z;
+            v[3] = t.w;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = c0 + j < cols ? __ldg(src + j) : 0.0f;
+        }
+        float h[4], l[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) tf32_split(v[j], h[j], l[j]);
+        float* dh = out + ((2 * b) * rows + r) * ldo + c0;
+        float* dl = out + ((2 * b + 1) * rows + r) * ldo + c0;
+        *reinterpret_cast<float4*>(dh) = make_float4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<float4*>(dl) = make_float4(l[0], l[1], l[2], l[3]);
+    }
+}
+
+// out[b][0 / 1][c][r] = hi / lo of X[b][r][c] (transposed through a 32 x 32
+// shared tile so both the loads and the stores are coalesced); columns
+// rows .. ldo-1 of out are zero.
+__global__ void __launch_bounds__(256) tf32_split_transpose_kernel(
+    const float* __restrict__ X, int64_t rows, int64_t cols, int64_t ld, int64_t bstride,
+    int64_t batches, float* __restrict__ out, int64_t ldo) {
+    __shared__ float t[32][33];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 32;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 32;
+    for (int64_t b = blockIdx.z; b < batches; b += gridDim.z) {
+        const float* src = X + b * bstride;
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+            const int64_t r = r0 + ty + j, c = c0 + tx;
+            t[ty + j][tx] = (r < rows && c < cols) ? __ldg(src + r * ld + c) : 0.0f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+            const int64_t c = c0 + ty + j, r = r0 + tx;  // output row c, column r
+            if (c < cols && r < ldo) {
+                float h, l;
+                tf32_split(t[tx][ty + j], h, l);
+                out[((2 * b) * cols + c) * ldo + r] = h;
+                out[((2 * b + 1) * cols + c) * ldo + r] = l;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+cudaError_t launch_tf32_split(const float* X, int64_t rows, int64_t cols, int64_t ld,
+                              int64_t bstride, int64_t batches, bool transpose, float* out,
+                              int64_t ldo, cudaStream_t stream) {
+    if (rows <= 0 || cols <= 0 || batches <= 0) return cudaSuccess;
+    if (ldo % 4 != 0 || reinterpret_cast<uintptr_t>(out) % 16 != 0) return cudaErrorInvalidValue;
+    if (!transpose) {
+        const int vec = reinterpret_cast<uintptr_t>(X) % 16 == 0 && ld % 4 == 0 &&
+                        (batches == 1 || bstride % 4 == 0);
+        const int64_t total = batches * rows * (ldo / 4);
+        int64_t blocks = (total + 255) / 256;
+        if (blocks > 4096) blocks = 4096;
+        tf32_split_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            X, rows, cols, ld, bstride, batches, vec, out, ldo);
+    } else {
+        const int64_t gx = (cols + 31) / 32, gy = (ldo + 31) / 32;
+        if (gx > 0x7fffffff || gy > 65535) return cudaErrorInvalidValue;
+        const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy),
+                        static_cast<unsigned>(batches < 65535 ? batches : 65535));
+        tf32_split_transpose_kernel<<<grid, 256, 0, stream>>>(X, rows, cols, ld, bstride, batches,
+                                                              out, ldo);
+    }
+    return cudaGetLastError();
+}
+
 cudaError_t launch_split_reduce(const float* partial, int64_t M, int64_t N, int64_t batch,
                                 int splits, const EpiParams& e, const LaunchCtx& lc) {
     SkinnyParams sp{};

@@ -70,6 +70,8 @@ struct gemm_plan_s {
     size_t sk_off = 0, sk_tags_off = 0;   // stream-K / split-K partial slots and tags in d_ws
     size_t sk_ctr_bytes = 0;              // skinny split-K arrival counters
     int64_t sk_grid = 0;
+    size_t t3_a_off = 0, t3_b_off = 0;    // 3xTF32 split buffers [batch][hi, lo][rows][t3_ld]
+    int64_t t3_ld = 0;
     std::atomic<unsigned> epoch{0};       // tag counter for stream-K launches
     std::mutex mu;                        // guards the descriptor cache
     const void* mapA_src = nullptr;
@@ -158,6 +160,7 @@ int kernels_per_run(const gemm_plan_s* pl) {
     const Problem& p = pl->p;
     if (p.M == 0 || p.N == 0) return 0;
     if (pl->cfg.kernel == GEMM_KERNEL_SKINNY) return 1;
+    if (pl->cfg.kernel == GEMM_KERNEL_TF32X3) return 3;  // split A, split B, GEMM
     return 1 + (pl->cfg.stage_a ? 1 : 0) + (pl->cfg.stage_b ? 1 : 0) +
            (tc_splits_of(pl) > 1 ? 1 : 0);
 }
@@ -178,6 +181,7 @@ int make_plan(const Problem& p, const gemm_config_t* forced, gemm_plan_t* out_pl
     int rc = forced ? check_config(p, *forced, &cfg) : cached_config(p, sms, &cfg, &hit);
     if (rc != GEMM_OK) return rc;
     if (cfg.kernel == GEMM_KERNEL_TC && tc_smem_bytes(cfg) == 0) return GEMM_ERR_UNSUPPORTED;
+    if (cfg.kernel == GEMM_KERNEL_TF32X3 && tc3_smem_bytes(cfg) == 0) return GEMM_ERR_UNSUPPORTED;
     if (cfg.kernel == GEMM_KERNEL_FFMA && ffma_smem_bytes(cfg) == 0) return GEMM_ERR_UNSUPPORTED;
     if (cfg.kernel == GEMM_KERNEL_FFMA &&
         !ffma_units_ok(Shape{p.M, p.N, p.K, p.epi.batch, 1, 1}, cfg.bn))
@@ -207,6 +211,14 @@ int make_plan(const Problem& p, const gemm_config_t* forced, gemm_plan_t* out_pl
         pl->ldb_s = round_up(std::max<int64_t>(g.cols, 1), pad);
         pl->stride_bs = g.rows * pl->ldb_s;
         ws += static_cast<size_t>(round_up(g.batches * pl->stride_bs * esz, 256));
+    }
+    if (cfg.kernel == GEMM_KERNEL_TF32X3) {
+        // hi / lo TF32 parts of A ([M][K]) and of B as [N][K], rows padded to 16 bytes
+        pl->t3_ld = round_up(std::max<int64_t>(p.K, 1), 4);
+        pl->t3_a_off = ws;
+        ws += static_cast<size_t>(round_up(geom_a(p).batches * 2 * p.M * pl->t3_ld * 4, 256));
+        pl->t3_b_off = ws;
+        ws += static_cast<size_t>(round_up(geom_b(p).batches * 2 * p.N * pl->t3_ld * 4, 256));
     }
     if (cfg.kernel == GEMM_KERNEL_TC && tc_effective_splits(p.K, cfg.split_k) > 1) {
         // split-K partial slabs: [batch][splits][M][N] FP32
@@ -383,8 +395,40 @@ int gemm_run(gemm_plan_t plan, const void* A, const void* B, void* C, const void
         return map_cuda_error(ce);
     }
 
-    // Effective (possibly staged) operands for the TMA kernels.
     const OperandGeom ga = geom_a(p), gb = geom_b(p);
+    CUtensorMap mA, mB;
+    if (cfg.kernel == GEMM_KERNEL_TF32X3) {
+        // Split both operands into TF32 hi / lo parts (B transposed to [N][K]
+        // when it comes as KN), then the tensor-core kernel reads the parts.
+        float* wa = reinterpret_cast<float*>(static_cast<char*>(plan->d_ws) + plan->t3_a_off);
+        float* wb = reinterpret_cast<float*>(static_cast<char*>(plan->d_ws) + plan->t3_b_off);
+        const int64_t ldt = plan->t3_ld;
+        ce = launch_tf32_split(static_cast<const float*>(A), ga.rows, ga.cols, ga.ld, ga.bstride,
+                               ga.batches, false, wa, ldt, st);
+        if (ce == cudaSuccess)
+            ce = launch_tf32_split(static_cast<const float*>(B), gb.rows, gb.cols, gb.ld,
+                                   gb.bstride, gb.batches, ep.b_layout == GEMM_B_KN, wb, ldt, st);
+        if (ce != cudaSuccess) return map_cuda_error(ce);
+        s.a_bmul = ga.batches > 1 ? 1 : 0;
+        s.b_bmul = gb.batches > 1 ? 1 : 0;
+        std::lock_guard<std::mutex> lk(plan->mu);
+        if (plan->mapA_src != wa) {
+            int rc = encode(&plan->mapA, GEMM_F32, wa, p.K, p.M, ldt, 2 * ga.batches, p.M * ldt,
+                            32, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+            if (rc == GEMM_OK)
+                rc = encode(&plan->mapB, GEMM_F32, wb, p.K, p.N, ldt, 2 * gb.batches, p.N * ldt,
+                            32, static_cast<uint32_t>(tc_b_box_rows(cfg)),
+                            CU_TENSOR_MAP_SWIZZLE_128B);
+            if (rc != GEMM_OK) {
+                plan->mapA_src = nullptr;
+                return rc;
+            }
+            plan->mapA_src = wa;
+        }
+        mA = plan->mapA;
+        mB = plan->mapB;
+    } else {
+    // Effective (possibly staged) operands for the TMA kernels.
     const void* a_src = A;
     const void* b_src = B;
     int64_t lda = p.lda, ldb = p.ldb;
@@ -411,7 +455,6 @@ int gemm_run(gemm_plan_t plan, const void* A, const void* B, void* C, const void
     s.a_bmul = ga.batches > 1 ? 1 : 0;
     s.b_bmul = gb.batches > 1 ? 1 : 0;
 
-    CUtensorMap mA, mB;
     {
         std::lock_guard<std::mutex> lk(plan->mu);
         if (plan->mapA_src != a_src || plan->mapB_src != b_src) {
@@ -445,7 +488,8 @@ int gemm_run(gemm_plan_t plan, const void* A, const void* B, void* C, const void
         mA = plan->mapA;
         mB = plan->mapB;
     }
-    if (cfg.kernel != GEMM_KERNEL_TC) {
+    }
+    if (cfg.kernel == GEMM_KERNEL_FFMA) {
         ce = launch_ffma(cfg, ep.b_layout, mA, mB, s, e, lc);
         return map_cuda_error(ce);
     }
@@ -528,7 +572,10 @@ int gemm_run(gemm_plan_t plan, const void* A, const void* B, void* C, const void
             }
         }
     }
-    ce = launch_tc(cfg, p.dtype, ep.b_layout, mA, mB, use_em ? &em : nullptr, s, e, lc);
+    if (cfg.kernel == GEMM_KERNEL_TF32X3)
+        ce = launch_tc3(cfg, mA, mB, use_em ? &em : nullptr, s, e, lc);
+    else
+        ce = launch_tc(cfg, p.dtype, ep.b_layout, mA, mB, use_em ? &em : nullptr, s, e, lc);
     return map_cuda_error(ce);
 }
 

@@ -29,7 +29,7 @@ namespace {
 constexpr int64_t kSkinnyMax = 4;
 
 std::mutex g_cache_mu;
-std::map<std::array<int64_t, 19>, gemm_config_t> g_cache;
+std::map<std::array<int64_t, 20>, gemm_config_t> g_cache;
 int64_t g_hits = 0, g_misses = 0;
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -179,6 +179,21 @@ int choose_config(const Problem& p, int num_sms, gemm_config_t* out) {
         *out = c;
         return GEMM_OK;
     }
+    if (p.dtype == GEMM_F32 && (p.epi.flags & GEMM_FLAG_FP32_TENSOR) && K >= 256 &&
+        bt * M * N >= (int64_t(1) << 20)) {
+        // 3xTF32 on the tensor cores: three TF32 MMAs per K step at half the
+        // BF16 rate, after an HBM-bound split pass over A and B.
+        c.kernel = GEMM_KERNEL_TF32X3;
+        c.bm = 128;
+        c.bk = 32;
+        c.stages = 3;
+        const bool pair = M > 128 && N > 128 && num_sms >= 2;
+        c.bn = pair ? 256 : 128;
+        c.variant = pair ? TC_VARIANT_PAIR : 0;
+        c.raster_group = static_cast<int32_t>(std::min<int64_t>(16, cdiv(M, pair ? 256 : 128)));
+        *out = c;
+        return GEMM_OK;
+    }
     if (p.dtype == GEMM_F32) {
         c.kernel = GEMM_KERNEL_FFMA;
         c.bm = 128;
@@ -271,6 +286,17 @@ int check_config(const Problem& p, const gemm_config_t& in, gemm_config_t* out) 
             if (c.stages < 2 || c.stages > 4) return GEMM_ERR_UNSUPPORTED;
             if (c.raster_group == 0) c.raster_group = 8;
             break;
+        case GEMM_KERNEL_TF32X3:
+            // (BN, variant): (256, 2) CTA pairs or (128, 0) single CTAs, 3 stages
+            if (p.dtype != GEMM_F32 || p.K == 0) return GEMM_ERR_UNSUPPORTED;
+            if (c.stream_k != 0 || c.split_k > 1) return GEMM_ERR_UNSUPPORTED;
+            if (c.bm != 128 || c.bk != 32 || c.stages != 3) return GEMM_ERR_UNSUPPORTED;
+            if (!((c.bn == 256 && c.variant == TC_VARIANT_PAIR) || (c.bn == 128 && c.variant == 0)))
+                return GEMM_ERR_UNSUPPORTED;
+            c.stage_a = c.stage_b = 0;  // the split pass reads any stride and alignment
+            if (c.raster_group == 0) c.raster_group = 16;
+            *out = c;
+            return GEMM_OK;
         case GEMM_KERNEL_TC:
             if (p.dtype == GEMM_F32 || p.K == 0) return GEMM_ERR_UNSUPPORTED;
             if (c.stream_k != 0) return GEMM_ERR_UNSUPPORTED;
@@ -302,10 +328,11 @@ int check_config(const Problem& p, const gemm_config_t& in, gemm_config_t* out) 
 
 int cached_config(const Problem& p, int num_sms, gemm_config_t* out, bool* hit) {
     const gemm_epilogue_t& e = p.epi;
-    const std::array<int64_t, 19> key = {
+    const std::array<int64_t, 20> key = {
         p.dtype,   p.M,        p.N,        p.K,        p.lda,        p.ldb,   p.ldc,
         e.b_layout, e.out_dtype, e.has_bias, e.act,    e.has_residual, e.ldr, e.batch,
-        e.stride_a, e.stride_b, e.stride_c, e.stride_r, num_sms};
+        e.stride_a, e.stride_b, e.stride_c, e.stride_r, num_sms,
+        static_cast<int64_t>(e.flags & GEMM_FLAG_FP32_TENSOR)};
     {
         std::lock_guard<std::mutex> lk(g_cache_mu);
         auto it = g_cache.find(key);

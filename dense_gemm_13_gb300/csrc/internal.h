@@ -68,6 +68,19 @@ cudaError_t launch_split_reduce(const float* partial, int64_t M, int64_t N, int6
                                 int splits, const EpiParams& e, const LaunchCtx& lc);
 // Shared memory the TC kernel needs for a config (bytes), or 0 if unsupported.
 size_t tc_smem_bytes(const gemm_config_t& cfg);
+// FP32 on the tensor cores (3xTF32): A and B come as split buffers
+// [batch][hi, lo][rows][K] (B K-major), tmA / tmB over (K, rows, 2 * batch).
+cudaError_t launch_tc3(const gemm_config_t& cfg, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                       const TcEpiMaps* em, const Shape& s, const EpiParams& e,
+                       const LaunchCtx& lc);
+size_t tc3_smem_bytes(const gemm_config_t& cfg);
+// Splits FP32 X[batch][rows][cols] (row stride ld, batch stride bstride,
+// any alignment) into out[batch][2][cols or rows][ldo]: hi = X rounded to
+// TF32 (nearest), lo = X - hi.  transpose: out rows are X's columns (for B
+// in KN layout); columns past the source's are written as zeros up to ldo.
+cudaError_t launch_tf32_split(const float* X, int64_t rows, int64_t cols, int64_t ld,
+                              int64_t bstride, int64_t batches, bool transpose, float* out,
+                              int64_t ldo, cudaStream_t stream);
 // TC config variant that runs CTA pairs (tcgen05 cta_group::2, 256-row tiles).
 constexpr int TC_VARIANT_PAIR = 2;
 // Rows of a K-major B box: the tile's columns, split between the CTAs of a pair.

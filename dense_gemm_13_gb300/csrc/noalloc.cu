@@ -145,6 +145,7 @@ extern "C" int gemm_run_noalloc(gemm_dtype_t dtype, int64_t M, int64_t N, int64_
     if (major != 10 || minor != 3) return GEMM_ERR_NO_DEVICE;
 
     gemm_config_t cfg;
+    p.epi.flags &= ~GEMM_FLAG_FP32_TENSOR;  // 3xTF32 needs split buffers: FP32 runs on FFMA
     rc = choose_config(p, sms, &cfg);  // no cache: nothing is allocated, not even on the host
     if (rc != GEMM_OK) return rc;
     cfg.stream_k = 0;  // whole tiles per CTA: stream-K partial slots would need more scratch
@@ -247,7 +248,7 @@ extern "C" int gemm_run_noalloc(gemm_dtype_t dtype, int64_t M, int64_t N, int64_
                             CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc == GEMM_OK)
             rc = noalloc_encode(&mB, p.dtype, b_src, b_cols, b_rows, lb, b_bat, sb, 64,
-                                kn ? 64u : static_cast<uint32_t>(cfg.bn),
+                                kn ? 64u : static_cast<uint32_t>(tc_b_box_rows(cfg)),
                                 CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc != GEMM_OK) return rc;
         return status_of(launch_tc(cfg, p.dtype, ep.b_layout, mA, mB, nullptr, s, e, lc));

@@ -54,16 +54,22 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
-constexpr int TBM = 128, TBK = 64;
-constexpr int T_A_BYTES = TBM * TBK * 2;  // 16 KB: 128 rows x 128 B
+constexpr int TBM = 128, TBK = 64;        // rows of A per CTA; K elements per stage (16-bit)
+constexpr int TBK3 = 32;                   // K elements per stage for FP32 (3xTF32)
+constexpr int T_A_TILE = TBM * 128;        // 16 KB: 128 rows x 128 B (64 x 16-bit or 32 x FP32)
 constexpr int EPI_BUF_BYTES = 32 * 128;   // one 32-row x 128-byte output (or residual) chunk
 
-template <int BN, bool PAIR>
+// K3: FP32 inputs as 3xTF32 -- each stage holds the high and the low TF32
+// parts of the A and B boxes: [A hi | A lo | B hi | B lo].
+template <int BN, bool PAIR, bool K3>
 struct TcLayout {
-    static constexpr int B_ROWS = PAIR ? BN / 2 : BN;   // B columns this CTA loads
-    static constexpr int B_BYTES = B_ROWS * TBK * 2;    // B_ROWS x 128 B
-    static constexpr int STAGE_BYTES = T_A_BYTES + B_BYTES;
-    static constexpr int TILE_M = PAIR ? 2 * TBM : TBM; // rows of a (pair) tile
+    static constexpr int KE = K3 ? TBK3 : TBK;           // K elements per stage
+    static constexpr int B_ROWS = PAIR ? BN / 2 : BN;    // B columns this CTA loads
+    static constexpr int B_TILE = B_ROWS * 128;          // B_ROWS x 128 B
+    static constexpr int A_BYTES = T_A_TILE * (K3 ? 2 : 1);
+    static constexpr int B_BYTES = B_TILE * (K3 ? 2 : 1);
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int TILE_M = PAIR ? 2 * TBM : TBM;  // rows of a (pair) tile
 };
 
 struct TcArgs {
@@ -96,19 +102,19 @@ template <int EW>
 __host__ __device__ constexpr int tc_threads() {
     return 64 + 32 * EW;
 }
-template <int BN, int STAGES, bool PAIR>
+template <int BN, int STAGES, bool PAIR, bool K3>
 __host__ __device__ constexpr int tc_epi_off() {
-    return STAGES * TcLayout<BN, PAIR>::STAGE_BYTES;
+    return STAGES * TcLayout<BN, PAIR, K3>::STAGE_BYTES;
 }
-template <int BN, int STAGES, int EW, bool PAIR>
+template <int BN, int STAGES, int EW, bool PAIR, bool K3>
 __host__ __device__ constexpr int tc_bar_off() {
-    return tc_epi_off<BN, STAGES, PAIR>() + EW * 2 * EPI_BUF_BYTES;
+    return tc_epi_off<BN, STAGES, PAIR, K3>() + EW * 2 * EPI_BUF_BYTES;
 }
-template <int BN, int STAGES, int EW, bool PAIR>
+template <int BN, int STAGES, int EW, bool PAIR, bool K3>
 __host__ __device__ constexpr int tc_smem_total() {
     // ring + epilogue tiles + full/empty per stage + tfull/tempty x2 + drain
     // + residual barriers (2 per epilogue warp) + tmem slot + abort flag
-    return 1024 + tc_bar_off<BN, STAGES, EW, PAIR>() + (2 * STAGES + 5 + 2 * EW) * 8 + 16;
+    return 1024 + tc_bar_off<BN, STAGES, EW, PAIR, K3>() + (2 * STAGES + 5 + 2 * EW) * 8 + 16;
 }
 
 __device__ __forceinline__ void tc_tile_coords(int64_t t, const TcArgs& a, int64_t& b, int64_t& mt,
@@ -130,17 +136,18 @@ __device__ __forceinline__ void tc_drain(uint32_t bar, uint32_t parity, uint64_t
         if (globaltimer_ns() - t0 > timeout_ns) return;
 }
 
-template <int BN, int STAGES, bool B_KN, int EW, bool PAIR>
+template <int BN, int STAGES, bool B_KN, int EW, bool PAIR, bool K3>
 __global__ void __launch_bounds__(tc_threads<EW>(), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmR,
                    const TcArgs args) {
-    using L = TcLayout<BN, PAIR>;
+    using L = TcLayout<BN, PAIR, K3>;
+    static_assert(!(K3 && B_KN), "3xTF32 reads B K-major (the split pass transposes KN)");
     constexpr uint32_t TMEM_COLS = 2 * BN;  // 256 or 512: powers of two
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + tc_bar_off<BN, STAGES, EW, PAIR>());
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + tc_bar_off<BN, STAGES, EW, PAIR, K3>());
     uint64_t* empty = full + STAGES;
     uint64_t* tfull = empty + STAGES;
     uint64_t* tempty = tfull + 2;
@@ -214,9 +221,10 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                     const bool skip = stall && t == first_item && kb == kb_lo;
                     if (!skip) {
                         uint8_t* sa = smem + s * L::STAGE_BYTES;
-                        uint8_t* sb = sa + T_A_BYTES;
-                        const int32_t ba = static_cast<int32_t>(b * args.a_bmul);
-                        const int32_t bb = static_cast<int32_t>(b * args.b_bmul);
+                        uint8_t* sb = sa + L::A_BYTES;
+                        // 3xTF32: the split buffers hold [batch][hi, lo][rows][K]
+                        const int32_t ba = static_cast<int32_t>(b * args.a_bmul) * (K3 ? 2 : 1);
+                        const int32_t bb = static_cast<int32_t>(b * args.b_bmul) * (K3 ? 2 : 1);
                         // In a pair, both CTAs' boxes for stage s land on the even
                         // CTA's full[s], which expects both CTAs' bytes.
                         const uint32_t bar =
@@ -231,13 +239,17 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                             else
                                 tma_load_3d(dst, m, bar, c0, c1, c2);
                         };
-                        load(smem_u32(sa), &tmA, kb * TBK, m0, ba);
-                        if (B_KN) {
+                        load(smem_u32(sa), &tmA, kb * L::KE, m0, ba);
+                        if (K3) {
+                            load(smem_u32(sa + T_A_TILE), &tmA, kb * L::KE, m0, ba + 1);
+                            load(smem_u32(sb), &tmB, kb * L::KE, n0, bb);
+                            load(smem_u32(sb + L::B_TILE), &tmB, kb * L::KE, n0, bb + 1);
+                        } else if (B_KN) {
 #pragma unroll
                             for (int j = 0; j < L::B_ROWS / 64; ++j)
-                                load(smem_u32(sb + j * (64 * 128)), &tmB, n0 + 64 * j, kb * TBK, bb);
+                                load(smem_u32(sb + j * (64 * 128)), &tmB, n0 + 64 * j, kb * L::KE, bb);
                         } else {
-                            load(smem_u32(sb), &tmB, kb * TBK, n0, bb);
+                            load(smem_u32(sb), &tmB, kb * L::KE, n0, bb);
                         }
                         armed |= 1u << s;
                         armed_par = (armed_par & ~(1u << s)) | (ph << s);
@@ -294,9 +306,31 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                     }
                     tc_fence_after();
                     const uint32_t sa = smem_u32(smem + s * L::STAGE_BYTES);
-                    const uint32_t sb = sa + T_A_BYTES;
+                    const uint32_t sb = sa + L::A_BYTES;
+                    if (K3) {
+                        // 3xTF32: per 8-deep K step, A.B ~ Alo.Bhi + Ahi.Blo + Ahi.Bhi
+                        // (the small terms first); a K step of 8 FP32 is 32 B
+                        // inside the swizzled 128-byte row, as for 16-bit inputs.
 #pragma unroll
-                    for (int kk = 0; kk < TBK / 16; ++kk) {
+                        for (int kk = 0; kk < L::KE / 8; ++kk) {
+                            const uint64_t ah = smem_desc_sw128(sa + kk * 32, 16, 1024);
+                            const uint64_t al = smem_desc_sw128(sa + T_A_TILE + kk * 32, 16, 1024);
+                            const uint64_t bh = smem_desc_sw128(sb + kk * 32, 16, 1024);
+                            const uint64_t bl = smem_desc_sw128(sb + L::B_TILE + kk * 32, 16, 1024);
+                            const uint32_t acc = ((kb - kb_lo) | kk) != 0 ? 1u : 0u;
+                            if (PAIR) {
+                                tc_mma_tf32_pair(d_tmem, al, bh, args.idesc, acc);
+                                tc_mma_tf32_pair(d_tmem, ah, bl, args.idesc, 1u);
+                                tc_mma_tf32_pair(d_tmem, ah, bh, args.idesc, 1u);
+                            } else {
+                                tc_mma_tf32(d_tmem, al, bh, args.idesc, acc);
+                                tc_mma_tf32(d_tmem, ah, bl, args.idesc, 1u);
+                                tc_mma_tf32(d_tmem, ah, bh, args.idesc, 1u);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < (K3 ? 0 : TBK / 16); ++kk) {
                         // A: K-major, rows of 128 B, 8-row swizzle atoms 1024 B apart;
                         // a K step of 16 elements is 32 B inside the swizzled row.
                         const uint64_t adesc = smem_desc_sw128(sa + kk * 32, 16, 1024);
@@ -350,7 +384,7 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
         constexpr int SLICE = BN / (EW / 4);
         const int c_lo = (ew >> 2) * SLICE;
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-        uint8_t* etile = smem + tc_epi_off<BN, STAGES, PAIR>() + ew * 2 * EPI_BUF_BYTES;
+        uint8_t* etile = smem + tc_epi_off<BN, STAGES, PAIR, K3>() + ew * 2 * EPI_BUF_BYTES;
         // Hand an accumulator buffer back to the MMA thread (the even CTA's in a pair).
         const auto release = [&](int buf) {
             tc_fence_before();
@@ -564,11 +598,11 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
     }
 }
 
-template <int BN, int STAGES, bool B_KN, int EW, bool PAIR>
+template <int BN, int STAGES, bool B_KN, int EW, bool PAIR, bool K3>
 cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& tmA,
                         const CUtensorMap& tmB, const TcEpiMaps* em, const Shape& s,
                         const EpiParams& e, const LaunchCtx& lc, const EpiParams* final_epi) {
-    using L = TcLayout<BN, PAIR>;
+    using L = TcLayout<BN, PAIR, K3>;
     TcArgs a{};
     a.M = s.M;
     a.N = s.N;
@@ -589,15 +623,16 @@ cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& 
     a.n_tiles = (s.N + BN - 1) / BN;
     a.tiles_per_batch = a.m_tiles * a.n_tiles;
     a.total_tiles = a.tiles_per_batch * s.batch;
-    a.k_blocks = static_cast<int>((s.K + TBK - 1) / TBK);
-    a.splits = PAIR ? 1 : tc_effective_splits(s.K, cfg.split_k);
+    a.k_blocks = static_cast<int>((s.K + L::KE - 1) / L::KE);
+    a.splits = (PAIR || K3) ? 1 : tc_effective_splits(s.K, cfg.split_k);
     a.kb_per_split = (a.k_blocks + a.splits - 1) / a.splits;
     a.total_items = a.total_tiles * a.splits;
     a.raster = cfg.raster_group > 0 ? cfg.raster_group : 16;
-    // Instruction descriptor, kind::f16: D = F32 (bits 4-5 = 1); A and B type
-    // (bits 7-9, 10-12) 0 = F16, 1 = BF16; A K-major (bit 15 = 0); B K-major
-    // (bit 16 = 0) or MN-major (1); N >> 3 at bits 17-22; M >> 4 at bits 24-28.
-    const uint32_t ab = dtype == GEMM_BF16 ? 1u : 0u;
+    // Instruction descriptor, kind::f16 / kind::tf32: D = F32 (bits 4-5 = 1);
+    // A and B type (bits 7-9, 10-12) 0 = F16, 1 = BF16, 2 = TF32; A K-major
+    // (bit 15 = 0); B K-major (bit 16 = 0) or MN-major (1); N >> 3 at bits
+    // 17-22; M >> 4 at bits 24-28.
+    const uint32_t ab = K3 ? 2u : dtype == GEMM_BF16 ? 1u : 0u;
     a.idesc = (1u << 4) | (ab << 7) | (ab << 10) | ((B_KN ? 1u : 0u) << 16) |
               (static_cast<uint32_t>(BN >> 3) << 17) |
               (static_cast<uint32_t>(L::TILE_M >> 4) << 24);
@@ -605,8 +640,8 @@ cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& 
     a.status = lc.status;
     a.timeout_ns = lc.timeout_ns;
     a.flags = lc.flags;
-    const int smem = tc_smem_total<BN, STAGES, EW, PAIR>();
-    auto kern = tc_gemm_kernel<BN, STAGES, B_KN, EW, PAIR>;
+    const int smem = tc_smem_total<BN, STAGES, EW, PAIR, K3>();
+    auto kern = tc_gemm_kernel<BN, STAGES, B_KN, EW, PAIR, K3>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     const CUtensorMap& mc = em ? em->c : unused_map;
@@ -676,19 +711,45 @@ cudaError_t launch_tc_layout(const gemm_config_t& cfg, int dtype, const CUtensor
                              const EpiParams& e, const LaunchCtx& lc, const EpiParams* fe) {
 #define G13_TC_LAUNCH(BN, ST, EW, VAR, PAIR)                                             \
     if (cfg.bn == BN && cfg.stages == ST && cfg.variant == VAR)                          \
-        return launch_tc_t<BN, ST, B_KN, EW, PAIR>(cfg, dtype, tmA, tmB, em, s, e, lc, fe);
+        return launch_tc_t<BN, ST, B_KN, EW, PAIR, false>(cfg, dtype, tmA, tmB, em, s, e, lc, fe);
     G13_TC_CONFIGS(G13_TC_LAUNCH)
 #undef G13_TC_LAUNCH
     return cudaErrorInvalidValue;
 }
 
+// 3xTF32 configurations: (BN, STAGES, epilogue warps, variant, pair); 64 KB stages.
+#define G13_TC3_CONFIGS(X)   \
+    X(256, 3, 4, 2, true)    \
+    X(128, 3, 4, 0, false)
+
 }  // namespace
+
+cudaError_t launch_tc3(const gemm_config_t& cfg, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                       const TcEpiMaps* em, const Shape& s, const EpiParams& e,
+                       const LaunchCtx& lc) {
+#define G13_TC3_LAUNCH(BN, ST, EW, VAR, PAIR)                                              \
+    if (cfg.bn == BN && cfg.stages == ST && cfg.variant == VAR)                            \
+        return launch_tc_t<BN, ST, false, EW, PAIR, true>(cfg, GEMM_F32, tmA, tmB, em, s, e, lc, \
+                                                          nullptr);
+    G13_TC3_CONFIGS(G13_TC3_LAUNCH)
+#undef G13_TC3_LAUNCH
+    return cudaErrorInvalidValue;
+}
+
+size_t tc3_smem_bytes(const gemm_config_t& cfg) {
+#define G13_TC3_SMEM(BN, ST, EW, VAR, PAIR)                     \
+    if (cfg.bn == BN && cfg.stages == ST && cfg.variant == VAR) \
+        return tc_smem_total<BN, ST, EW, PAIR, true>();
+    G13_TC3_CONFIGS(G13_TC3_SMEM)
+#undef G13_TC3_SMEM
+    return 0;
+}
 
 size_t tc_smem_bytes(const gemm_config_t& cfg) {
     if (cfg.bm != TBM || cfg.bk != TBK) return 0;
 #define G13_TC_SMEM(BN, ST, EW, VAR, PAIR)                      \
     if (cfg.bn == BN && cfg.stages == ST && cfg.variant == VAR) \
-        return tc_smem_total<BN, ST, EW, PAIR>();
+        return tc_smem_total<BN, ST, EW, PAIR, false>();
     G13_TC_CONFIGS(G13_TC_SMEM)
 #undef G13_TC_SMEM
     return 0;
@@ -711,5 +772,6 @@ cudaError_t launch_tc(const gemm_config_t& cfg, int dtype, int b_layout, const C
 }
 
 #undef G13_TC_CONFIGS
+#undef G13_TC3_CONFIGS
 
 }  // namespace g13

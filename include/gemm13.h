@@ -68,6 +68,10 @@ typedef enum {
 } gemm_status_t;
 
 /* Plan flags (gemm_epilogue_t.flags). */
+#define GEMM_FLAG_FP32_TENSOR 0x1u       /* FP32 inputs: the dispatcher may pick the 3xTF32
+                                            tensor-core kernel (GEMM_KERNEL_TF32X3) for large
+                                            problems instead of the CUDA-core FFMA kernel; the
+                                            result meets the same tolerance */
 #define GEMM_FLAG_TEST_STALL 0x80000000u /* test only: the first CTA's producer withholds one
                                             operand tile so its waits run out; with a short
                                             timeout_ms this exercises the timeout path */
@@ -99,7 +103,14 @@ typedef enum {
     GEMM_KERNEL_AUTO = 0,   /* let the dispatcher choose */
     GEMM_KERNEL_TC = 1,     /* tcgen05 tensor cores, TMA + mbarrier ring, TMEM accumulators (16-bit in) */
     GEMM_KERNEL_FFMA = 2,   /* CUDA-core FP32 FFMA, TMA-fed (FP32 in) */
-    GEMM_KERNEL_SKINNY = 3  /* memory-bound kernel for M or N <= 64 (any input type) */
+    GEMM_KERNEL_SKINNY = 3, /* memory-bound streaming kernel for small M or N (any input type;
+                               the dispatcher uses it for min(M, N) <= 4 and for K == 0) */
+    GEMM_KERNEL_TF32X3 = 4  /* FP32 in on the tensor cores (tcgen05 kind::tf32): each operand
+                               is split x = hi + lo into two TF32 numbers by a pre-pass and
+                               A.B ~ Ahi.Bhi + Ahi.Blo + Alo.Bhi (the "SGEMM ... 83% of cuBLAS"
+                               page, sec. 6, names the TF32 tensor-core path as the next step
+                               past FFMA; splitting recovers FP32-level accuracy).  Needs a plan
+                               workspace of 2 x (M + N) x K FP32 values per batch entry. */
 } gemm_kernel_t;
 
 /* A tile configuration: what the dispatcher chose, or what a caller forces. */
@@ -113,7 +124,10 @@ typedef struct {
     int32_t stage_b;      /* 1: B likewise */
     int32_t num_ctas;     /* persistent grid size; 0 = one per SM */
     int32_t variant;      /* family-specific main-loop variant; FFMA: 0 scalar FFMA,
-                             1 packed fma.rn.f32x2 (KN layout only) */
+                             1 packed fma.rn.f32x2 (KN layout only); TC: 0 single CTAs with
+                             4 epilogue warps, 1 single CTAs with 8 epilogue warps (short K),
+                             2 CTA pairs (cta_group::2, 256 x 256 tiles, no split-K);
+                             TF32X3: 0 single CTAs (bn 128), 2 CTA pairs (bn 256) */
     int32_t stream_k;     /* FFMA: 1 = persistent grid with (tile, K-step) units split evenly
                              over the CTAs; tiles cut between CTAs are summed in a fixed order
                              (deterministic).  Needs a plan workspace of grid x 64 KB. */

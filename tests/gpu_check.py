@@ -44,7 +44,7 @@ class Run:
 
     def __init__(self, w: Workload, tensors: dict | None = None, config: g13.Config | None = None,
                  seed: int = 0, guard: bool = True, a_offset: int = 0, b_offset: int = 0,
-                 plan: g13.Plan | None = None, ldc_pad: int = 0):
+                 plan: g13.Plan | None = None, ldc_pad: int = 0, flags: int = 0):
         self.w = w
         self.t = tensors if tensors is not None else w.make(seed)
         dev = torch.device("cuda")
@@ -72,7 +72,7 @@ class Run:
                           stride_a=(w.M * w.K if (bt > 1 and A.dim() == 3) else 0),
                           stride_b=(B.shape[-1] * B.shape[-2] if (bt > 1 and B.dim() == 3) else 0),
                           stride_c=self.cbuf.shape[-1] * self.cbuf.shape[-2] if bt > 1 else 0,
-                          stride_r=(M * N if (bt > 1 and w.residual) else 0))
+                          stride_r=(M * N if (bt > 1 and w.residual) else 0), flags=flags)
         if w.residual and N == 0:
             ep.ldr = 1
         self.plan = plan or g13.gemm_plan(w.dtype, M, N, w.K, lda, ldb, self.ldc, ep, config)

@@ -96,6 +96,68 @@ def test_tc_pair_epilogue_batched():
         full_check(Run(w, config=g13.Config("tc", 128, 256, 64, 4, variant=2), ldc_pad=1))
 
 
+# ---------------------------------------------------------------- 3xTF32 (FP32 on tensor cores)
+TF32X3_CONFIGS = [g13.Config("tf32x3", 128, 256, 32, 3, variant=2),
+                  g13.Config("tf32x3", 128, 128, 32, 3)]
+
+
+@pytest.mark.parametrize("cfg", TF32X3_CONFIGS, ids=lambda c: f"bn{c.bn}v{c.variant}")
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+@pytest.mark.parametrize("shape", [(300, 600, 300), (513, 129, 200), (17, 33, 101)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_tf32x3_exact_integer(cfg, layout, shape):
+    # small integers are TF32 numbers (lo = 0) and every sum is exact in FP32
+    w = _int_workload("f32", layout, *shape)
+    run = Run(w, config=cfg)
+    assert run.info["kernels_per_run"] == 3
+    C = run.run().result()
+    _, cref, _ = run.oracle()
+    assert np.array_equal(C, cref.reshape(C.shape)), f"{w.name} {cfg}"
+    assert run.guard_ok()
+    cfg2 = g13.Config(cfg.kernel, cfg.bm, cfg.bn, cfg.bk, cfg.stages, num_ctas=2, variant=cfg.variant)
+    assert np.array_equal(Run(w, tensors=run.t, config=cfg2).run().result(), C)
+
+
+@pytest.mark.parametrize("cfg", TF32X3_CONFIGS, ids=lambda c: f"bn{c.bn}v{c.variant}")
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+def test_tf32x3_needs_all_three_terms(cfg, layout):
+    # x = 1 + 2^-12 is not a TF32 number: hi = 1, lo = 2^-12.  C = K (1 + 2^-12)^2;
+    # dropping lo (one TF32 product) errs by 2K * 2^-12 and dropping one cross
+    # term by K * 2^-12, both beyond the 2e-4 * sum|ab| tolerance; the three
+    # terms leave only lo.lo = K * 2^-24.
+    M, N, K = 200, 300, 1000
+    x = 1.0 + 2.0 ** -12
+    A = torch.full((M, K), x, dtype=torch.float32)
+    B = torch.full((K, N) if layout == "kn" else (N, K), x, dtype=torch.float32)
+    w = Workload(f"tf32x3_pin_{layout}", "f32", M, N, K, b_layout=layout)
+    run = Run(w, tensors={"A": A, "B": B, "bias": None, "R": None}, config=cfg)
+    C = run.run().result()
+    run.check(C)
+    assert np.max(np.abs(C - K * x * x)) <= K * 2.0 ** -20
+
+
+def test_tf32x3_random_epilogue_batched():
+    for layout in ("kn", "nk"):
+        w = Workload(f"tf32x3_epi_{layout}", "f32", 700, 520, 1500, batch=2, b_layout=layout,
+                     bias=True, act="gelu", residual=True, beta=0.5, alpha=0.25)
+        for cfg in TF32X3_CONFIGS:
+            full_check(Run(w, config=cfg))
+        # shared B across the batch, odd ldc (per-thread epilogue stores)
+        t = w.make(3)
+        t["B"] = t["B"][0]
+        full_check(Run(w, tensors=t, config=TF32X3_CONFIGS[0], ldc_pad=1))
+
+
+def test_tf32x3_chosen_with_flag_at_4096():
+    w = WORKLOADS["sgemm_4096"]
+    run = Run(w, flags=g13.FLAG_FP32_TENSOR)
+    assert run.info["config"].kernel == "tf32x3"
+    C = run.run().result()
+    run.check(C, rows=boundary_indices(w.M), cols=boundary_indices(w.N))
+    run.freivalds(C)
+    assert Run(w, tensors=run.t).info["config"].kernel == "ffma"   # without the flag: FFMA
+
+
 @pytest.mark.parametrize("split", [2, 3, 7])
 @pytest.mark.parametrize("layout", ["kn", "nk"])
 @pytest.mark.parametrize("shape", [(17, 300, 2000), (200, 129, 1500), (1, 64, 4096)],

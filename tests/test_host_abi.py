@@ -130,6 +130,12 @@ def test_dispatch_buckets(lib):
     assert sel("f32", 1, 4096, 4096).kernel == "skinny"
     assert sel("bf16", 4, 4096, 4096).kernel == "skinny"
     assert sel("bf16", 5, 4096, 4096).kernel == "tc"       # tensor cores (+ split-K) from 5 rows
+    # FP32 on the tensor cores (3xTF32) only when the caller allows it
+    c = sel("f32", 4096, 4096, 4096, flags=g13.FLAG_FP32_TENSOR)
+    assert (c.kernel, c.bn, c.variant, c.stages, c.stage_a, c.stage_b) == ("tf32x3", 256, 2, 3, 0, 0)
+    assert sel("f32", 100, 4096, 4096, flags=g13.FLAG_FP32_TENSOR).bn == 128   # single CTAs
+    assert sel("f32", 256, 256, 256, flags=g13.FLAG_FP32_TENSOR).kernel == "ffma"  # too small
+    assert sel("bf16", 4096, 4096, 4096, flags=g13.FLAG_FP32_TENSOR).kernel == "tc"
 
 
 def test_dispatch_staging_follows_alignment(lib):

@@ -48,6 +48,9 @@ CASES = [
               dist_a="uniform", dist_b="uniform", dist_r="uniform"), 0, 3),
     # FP32, K-major B, bias + GELU, A base 4 bytes off: the FFMA kernel reads staged copies
     (Workload("noalloc_f32", "f32", 130, 70, 301, b_layout="nk", bias=True, act="gelu"), 1, 0),
+    # K-major B with K > 1024: the tensor-core kernel runs as CTA pairs (half-width B boxes)
+    (Workload("noalloc_pair_nk", "bf16", 2048, 2048, 1100, b_layout="nk", dist_a="uniform",
+              dist_b="uniform"), 0, 0),
 ]
 
 
@@ -56,6 +59,8 @@ def test_noalloc_matches_planned_path_twice_in_a_row():
     runs, outs = [], []
     for w, a_off, b_off in CASES:
         run = Run(w, seed=11, a_offset=a_off, b_offset=b_off)
+        if w.name == "noalloc_pair_nk":
+            assert run.info["config"].variant == 2      # the same choice the entry point makes
         C = torch.full(run.cbuf.shape, float("nan"), dtype=TORCH_OUT[w.out_dtype],
                        device="cuda")[:, 1:1 + w.M, 8:8 + w.N]
         rc = _noalloc_call(run, C, stream)
