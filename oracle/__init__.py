@@ -30,7 +30,7 @@ SOURCE = os.path.join(_HERE, "gemm_oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
 DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
-ACTS = {"none": 0, "gelu": 1, "relu": 2}
+ACTS = {"none": 0, "gelu": 1, "relu": 2, "softmax": 3}
 LAYOUTS = {"kn": 0, "nk": 1}
 
 

@@ -25,6 +25,10 @@
  *     y_ij   = alpha * s_ij  (+ bias[j])
  *     y_ij   = act(y_ij)          none | GELU (erf form) | ReLU
  *     y_ij  += beta * R[i,j]      (if a residual is given)
+ *   or, for the row softmax of the scaled scores (the attention step
+ *   Softmax(QK^T) of "CUDA Tile ... GEMM", sec. 2; no residual):
+ *     y_ij   = exp(t_ij - m_i) / sum_j' exp(t_ij' - m_i),
+ *     t_ij   = alpha * s_ij (+ bias[j]),  m_i = max_j t_ij  (all N columns)
  *     c_ij   = y_ij rounded to the output type, round-to-nearest-even
  *     S_ij   = sum_k |A[i,k] * Bhat[k,j]|    (scale of the rounding error)
  * Readings where the pages are silent: the epilogue order (scale, bias,
@@ -35,6 +39,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 #ifdef _OPENMP
 #include <omp.h>
@@ -48,6 +53,7 @@
 #define OR_ACT_NONE 0
 #define OR_ACT_GELU 1
 #define OR_ACT_RELU 2
+#define OR_ACT_SOFTMAX 3
 /* Layout of B. */
 #define OR_B_KN 0
 #define OR_B_NK 1
@@ -136,12 +142,60 @@ int oracle_max_threads(void)
 #endif
 }
 
+/* s = sum_k A[i,k] * Bhat[k,j] (k ascending) and sa = sum_k |A[i,k] * Bhat[k,j]|. */
+static void dot_ij(int dtype, int64_t K, int64_t i, int64_t j, const void* Abat, int64_t lda,
+                   const void* Bbat, int64_t ldb, int b_layout, double* s_out, double* sa_out)
+{
+    double s = 0.0, sa = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        double a = load_elem(Abat, dtype, i * lda + k);
+        double bv = load_elem(Bbat, dtype, b_layout == OR_B_KN ? k * ldb + j : j * ldb + k);
+        s += a * bv;
+        sa += fabs(a * bv);
+    }
+    *s_out = s;
+    *sa_out = sa;
+}
+
+/* One output row of the row softmax (every column is needed for the
+ * maximum and the sum, whichever columns are reported). */
+static void softmax_row(int dtype, int64_t N, int64_t K, int64_t i, const void* Abat,
+                        int64_t lda, const void* Bbat, int64_t ldb, int b_layout, double alpha,
+                        const float* bias, int out_dtype, const int64_t* cols, int64_t ncols,
+                        double* y_row, double* c_row, double* sabs_row, double* t, double* sa_all)
+{
+    for (int64_t j = 0; j < N; ++j) {
+        double s, sa;
+        dot_ij(dtype, K, i, j, Abat, lda, Bbat, ldb, b_layout, &s, &sa);
+        t[j] = alpha * s + (bias ? (double)bias[j] : 0.0);
+        sa_all[j] = sa;
+    }
+    double m = -INFINITY;
+    for (int64_t j = 0; j < N; ++j)
+        if (t[j] > m)
+            m = t[j];
+    double z = 0.0;
+    for (int64_t j = 0; j < N; ++j)
+        z += exp(t[j] - m);
+    for (int64_t c = 0; c < ncols; ++c) {
+        int64_t j = cols ? cols[c] : c;
+        double y = exp(t[j] - m) / z;
+        if (y_row)
+            y_row[c] = y;
+        if (c_row)
+            c_row[c] = oracle_round_to(out_dtype, y);
+        if (sabs_row)
+            sabs_row[c] = sa_all[j];
+    }
+}
+
 /*
  * Full or sampled reference.  rows/cols select which outputs to compute
  * (NULL = all M rows / all N columns); results are written densely as
  * [batch][nrows][ncols].  y_out gets the epilogue value before output
  * rounding, c_out the value rounded to out_dtype, sabs_out the sum of
- * |a*b| (each may be NULL).  Returns 0, or -1 on a bad argument.
+ * |a*b| (each may be NULL).  Returns 0, or -1 on a bad argument (the row
+ * softmax takes no residual).
  */
 int oracle_gemm(int dtype, int64_t M, int64_t N, int64_t K, int64_t batch,
                 const void* A, int64_t lda, int64_t stride_a,
@@ -159,6 +213,8 @@ int oracle_gemm(int dtype, int64_t M, int64_t N, int64_t K, int64_t batch,
     if (dtype != OR_F32 && dtype != OR_F16 && dtype != OR_BF16)
         return -1;
     if (b_layout != OR_B_KN && b_layout != OR_B_NK)
+        return -1;
+    if (act == OR_ACT_SOFTMAX && R)
         return -1;
     if (!rows)
         nrows = M;
@@ -186,16 +242,21 @@ int oracle_gemm(int dtype, int64_t M, int64_t N, int64_t K, int64_t batch,
         int esz = dtype == OR_F32 ? 4 : 2;
         const void* Abat = Ab + (size_t)(b * stride_a) * esz;
         const void* Bbat = Bb + (size_t)(b * stride_b) * esz;
+        if (act == OR_ACT_SOFTMAX) {
+            int64_t o = (b * nrows + r) * ncols;
+            double* t = (double*)malloc(sizeof(double) * (size_t)(2 * N + 1));
+            if (!t)
+                continue;
+            softmax_row(dtype, N, K, i, Abat, lda, Bbat, ldb, b_layout, alpha, bias, out_dtype,
+                        cols, ncols, y_out ? y_out + o : NULL, c_out ? c_out + o : NULL,
+                        sabs_out ? sabs_out + o : NULL, t, t + N);
+            free(t);
+            continue;
+        }
         for (int64_t c = 0; c < ncols; ++c) {
             int64_t j = cols ? cols[c] : c;
-            double s = 0.0, sa = 0.0;
-            for (int64_t k = 0; k < K; ++k) {
-                double a = load_elem(Abat, dtype, i * lda + k);
-                double bv = load_elem(Bbat, dtype,
-                                      b_layout == OR_B_KN ? k * ldb + j : j * ldb + k);
-                s += a * bv;
-                sa += fabs(a * bv);
-            }
+            double s, sa;
+            dot_ij(dtype, K, i, j, Abat, lda, Bbat, ldb, b_layout, &s, &sa);
             double y = alpha * s;
             if (bias)
                 y += (double)bias[j];

@@ -17,6 +17,10 @@ What pins what:
   * The epilogue order: hand-derived scalar chains (tests/golden).
   * Sampling, batching and strides: against the full / unbatched result.
   * The Freivalds vectors: against C @ x and S @ |x| of the full result.
+  * The row softmax: scipy's softmax of the float64 product (a library
+    routine), the two-column closed form (the logistic function), rows
+    summing to one, no overflow for large logits, invariance to a constant
+    shift of the bias, and sampled / batched outputs against the full ones.
 """
 from __future__ import annotations
 
@@ -267,6 +271,60 @@ def check_freivalds(o):
         assert np.allclose(w, s @ np.abs(x), rtol=1e-12, atol=0), lay
 
 
+def check_softmax(o):
+    from scipy.special import softmax
+    rng = np.random.default_rng(21)
+    # scipy's softmax of the float64 product, per-column bias, NK layout (Q.K^T)
+    M, N, K = 7, 11, 16
+    A = rng.standard_normal((M, K)).astype(np.float32)
+    B = rng.standard_normal((N, K)).astype(np.float32)
+    bias = rng.standard_normal(N).astype(np.float32)
+    t = 0.125 * (A.astype(np.float64) @ B.astype(np.float64).T) + bias.astype(np.float64)
+    y, c, sabs = o.gemm(A, B, b_layout="nk", alpha=0.125, bias=bias, act="softmax")
+    assert np.allclose(y, softmax(t, axis=1), rtol=1e-12, atol=0)
+    assert np.all(np.abs(y.sum(axis=1) - 1.0) <= 1e-14)
+    assert np.array_equal(c, y.astype(np.float32).astype(np.float64))
+    assert np.allclose(sabs, np.abs(A.astype(np.float64)) @ np.abs(B.astype(np.float64)).T,
+                       rtol=1e-14)
+    # two columns: p0 = 1 / (1 + exp(t1 - t0)); B = I (KN) makes t = A
+    A2 = np.array([[1.0, 2.0], [3.0, -1.0], [0.5, 0.5]], np.float32)
+    y, _, _ = o.gemm(A2, np.eye(2, dtype=np.float32), act="softmax")
+    p0 = 1.0 / (1.0 + np.exp(A2[:, 1].astype(np.float64) - A2[:, 0]))
+    assert np.allclose(y[:, 0], p0, rtol=1e-15) and np.allclose(y[:, 1], 1.0 - p0, rtol=1e-14)
+    # large logits (alpha = 1000): no overflow, one-hot at the row maximum
+    Ai = rng.integers(-4, 5, (5, 8)).astype(np.float32)
+    Bi = rng.integers(-4, 5, (8, 9)).astype(np.float32)
+    y, _, _ = o.gemm(Ai, Bi, alpha=1000.0, act="softmax")
+    prod = Ai.astype(np.float64) @ Bi.astype(np.float64)
+    assert np.all(np.isfinite(y)) and np.all(np.abs(y.sum(axis=1) - 1.0) <= 1e-14)
+    for i in range(5):
+        top = np.flatnonzero(prod[i] == prod[i].max())
+        assert np.allclose(y[i, top], 1.0 / len(top), rtol=1e-12)
+    # a constant added to every bias entry leaves p unchanged (eighths: the shift is exact)
+    bq = (rng.integers(-16, 17, N) / 8).astype(np.float32)
+    y1, _, _ = o.gemm(A, B, b_layout="nk", alpha=0.125, bias=bq, act="softmax")
+    y2, _, _ = o.gemm(A, B, b_layout="nk", alpha=0.125, bias=bq + np.float32(3.0), act="softmax")
+    assert np.allclose(y1, y2, rtol=1e-13, atol=0)
+    # sampled rows / columns still see the whole row; batches are independent
+    rows, cols = np.array([6, 0, 3]), np.array([10, 2, 5, 4])
+    ys, _, _ = o.gemm(A, B, b_layout="nk", alpha=0.125, bias=bq, act="softmax", rows=rows,
+                      cols=cols)
+    assert np.array_equal(ys, y1[np.ix_(rows, cols)])
+    Ab = rng.standard_normal((3, M, K)).astype(np.float32)
+    Bb = rng.standard_normal((3, N, K)).astype(np.float32)
+    yb, _, _ = o.gemm(Ab, Bb, b_layout="nk", alpha=0.5, act="softmax", out_dtype="bf16")
+    for b in range(3):
+        yo, _, _ = o.gemm(Ab[b], Bb[b], b_layout="nk", alpha=0.5, act="softmax")
+        assert np.array_equal(yb[b], yo)
+    # the row softmax takes no residual
+    try:
+        o.gemm(A, B, b_layout="nk", act="softmax", R=np.zeros((M, N), np.float32))
+    except Exception:
+        pass
+    else:
+        raise AssertionError("softmax with a residual was accepted")
+
+
 ALL_CHECKS = [check_decode, check_round, check_act, check_brute_force, check_identity_permutation,
               check_all_ones, check_transpose_identity, check_numpy_matmul, check_epilogue_chain,
-              check_sampling_batching, check_sabs, check_freivalds]
+              check_sampling_batching, check_sabs, check_freivalds, check_softmax]

@@ -17,8 +17,8 @@ from tests import oracle_pins
 MUTANTS = [
     ("dropped_term", "s += a * bv;", "if (k != K / 2) s += a * bv;"),
     ("bias_sign", "y += (double)bias[j];", "y -= (double)bias[j];"),
-    ("transposed_b", "b_layout == OR_B_KN ? k * ldb + j : j * ldb + k);\n                s += a * bv;",
-     "b_layout == OR_B_KN ? j * ldb + k : k * ldb + j);\n                s += a * bv;"),
+    ("transposed_b", "b_layout == OR_B_KN ? k * ldb + j : j * ldb + k);\n        s += a * bv;",
+     "b_layout == OR_B_KN ? j * ldb + k : k * ldb + j);\n        s += a * bv;"),
     ("dropped_beta", "y += beta * (double)R[", "y += (double)R["),
     ("act_before_bias",
      "            if (bias)\n                y += (double)bias[j];\n            y = oracle_act(act, y);",
@@ -28,8 +28,8 @@ MUTANTS = [
     ("f16_exponent", "ex - 25", "ex - 24"),
     ("bf16_precision", "round_rne(x, 8, -126", "round_rne(x, 7, -126"),
     ("sabs_signed", "sa += fabs(a * bv);", "sa += a * bv;"),
-    ("ignores_lda", "load_elem(Abat, dtype, i * lda + k);\n                double bv",
-     "load_elem(Abat, dtype, i * K + k);\n                double bv"),
+    ("ignores_lda", "load_elem(Abat, dtype, i * lda + k);\n        double bv",
+     "load_elem(Abat, dtype, i * K + k);\n        double bv"),
     ("residual_batch", "R[b * stride_r + i * ldr + j];\n            int64_t o",
      "R[i * ldr + j];\n            int64_t o"),
     ("freivalds_x", "s += bv * x[j];", "s += bv;"),
@@ -37,6 +37,13 @@ MUTANTS = [
     ("relu_abs", "y > 0.0 ? y : 0.0", "y > 0.0 ? y : -y"),
     ("f16_subnormal", "ldexp((double)fr, -24)", "ldexp((double)fr, -25)"),
     ("sample_rows", "int64_t i = rows ? rows[r] : r;", "int64_t i = r;"),
+    # row softmax
+    ("softmax_no_bias", "t[j] = alpha * s + (bias ? (double)bias[j] : 0.0);", "t[j] = alpha * s;"),
+    ("softmax_no_max", "z += exp(t[j] - m);", "z += exp(t[j]);"),
+    ("softmax_norm", "double y = exp(t[j] - m) / z;", "double y = exp(t[j] - m) / (z + 1e-3);"),
+    ("softmax_sampled_cols", "double* t = (double*)malloc(sizeof(double) * (size_t)(2 * N + 1));",
+     "N = ncols; double* t = (double*)malloc(sizeof(double) * (size_t)(2 * N + 1));"),
+    ("softmax_alpha_late", "t[j] = alpha * s + (bias", "t[j] = s + (bias"),
 ]
 
 
