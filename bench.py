@@ -445,7 +445,7 @@ def run_ours(args):
     if not args.no_extra:
         extra = []
         for name in ("bf16_8192", "bf16_4096", "ffn1_bf16", "ffn1_f16", "ffn2_bf16", "qkt_bf16",
-                     "sgemm_256", "sgemm_4096+3xtf32"):
+                     "qkt_softmax_bf16", "sgemm_256", "sgemm_4096+3xtf32"):
             if name == w.name:
                 continue
             base, _, mode = name.partition("+")

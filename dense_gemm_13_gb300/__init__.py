@@ -23,7 +23,7 @@ __all__ = ["Epilogue", "Config", "Plan", "GemmError", "gemm_plan", "gemm_run", "
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgemm13.so")
 
 DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
-ACTS = {"none": 0, "gelu": 1, "relu": 2}
+ACTS = {"none": 0, "gelu": 1, "relu": 2, "softmax": 3}
 LAYOUTS = {"kn": 0, "nk": 1}
 KERNELS = {"auto": 0, "tc": 1, "ffma": 2, "skinny": 3, "tf32x3": 4}
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}

@@ -54,7 +54,8 @@ int make_problem(gemm_dtype_t dtype, int64_t M, int64_t N, int64_t K, int64_t ld
     if (e.out_dtype != GEMM_F32 && e.out_dtype != GEMM_BF16 && e.out_dtype != GEMM_F16)
         return GEMM_ERR_INVALID_ARG;
     if (e.b_layout != GEMM_B_KN && e.b_layout != GEMM_B_NK) return GEMM_ERR_INVALID_ARG;
-    if (e.act != GEMM_ACT_NONE && e.act != GEMM_ACT_GELU_ERF && e.act != GEMM_ACT_RELU)
+    if (e.act != GEMM_ACT_NONE && e.act != GEMM_ACT_GELU_ERF && e.act != GEMM_ACT_RELU &&
+        e.act != GEMM_ACT_SOFTMAX)
         return GEMM_ERR_INVALID_ARG;
     if (e.has_bias != 0 && e.has_bias != 1) return GEMM_ERR_INVALID_ARG;
     if (e.has_residual != 0 && e.has_residual != 1) return GEMM_ERR_INVALID_ARG;
@@ -75,6 +76,11 @@ int make_problem(gemm_dtype_t dtype, int64_t M, int64_t N, int64_t K, int64_t ld
         return GEMM_ERR_INVALID_ARG;
     if (e.batch > 1 && M > 0 && N > 0 && e.stride_c < M * ldc) return GEMM_ERR_INVALID_ARG;
     if (e.timeout_ms == 0) e.timeout_ms = 2000;
+    // The row softmax runs in the tensor-core epilogue with a whole row (up to
+    // 512 FP32 accumulator columns) in one CTA's TMEM.
+    if (e.act == GEMM_ACT_SOFTMAX &&
+        (dtype == GEMM_F32 || N > 512 || (K == 0 && M > 0 && N > 0) || e.has_residual))
+        return GEMM_ERR_UNSUPPORTED;
     p->dtype = dtype;
     p->M = M;
     p->N = N;
@@ -168,6 +174,20 @@ int choose_config(const Problem& p, int num_sms, gemm_config_t* out) {
     c.split_k = 1;
     c.num_ctas = 0;
     const int64_t M = p.M, N = p.N, K = p.K, bt = p.epi.batch;
+    if (p.epi.act == GEMM_ACT_SOFTMAX && M > 0 && N > 0) {
+        // one tile spans the whole row: 256 columns (double-buffered TMEM) or
+        // 512 (single-buffered); 4 epilogue warps, one thread per row
+        c.kernel = GEMM_KERNEL_TC;
+        c.bm = 128;
+        c.bk = 64;
+        c.bn = N <= 256 ? 256 : 512;
+        c.stages = N <= 256 ? 4 : 2;
+        c.variant = 0;
+        c.raster_group = static_cast<int32_t>(std::min<int64_t>(16, cdiv(M, 128)));
+        set_staging(p, &c);
+        *out = c;
+        return GEMM_OK;
+    }
     if (M == 0 || N == 0 || K == 0 || std::min(M, N) <= kSkinnyMax) {
         c.kernel = GEMM_KERNEL_SKINNY;
         c.bm = 1;
@@ -271,6 +291,8 @@ int check_config(const Problem& p, const gemm_config_t& in, gemm_config_t* out) 
     if (c.split_k < 1 || (c.split_k != 1 && c.kernel == GEMM_KERNEL_FFMA) || c.split_k > 1024)
         return GEMM_ERR_UNSUPPORTED;
     if (c.num_ctas < 0 || c.raster_group < 0) return GEMM_ERR_INVALID_ARG;
+    if (p.epi.act == GEMM_ACT_SOFTMAX && c.kernel != GEMM_KERNEL_TC && p.M > 0 && p.N > 0)
+        return GEMM_ERR_UNSUPPORTED;
     switch (c.kernel) {
         case GEMM_KERNEL_SKINNY:
             c.stage_a = c.stage_b = 0;
@@ -304,12 +326,19 @@ int check_config(const Problem& p, const gemm_config_t& in, gemm_config_t* out) 
             // (BN, stages) pairs with 4 epilogue warps (variant 0) or 8 (variant 1);
             // variant 2: CTA pairs on 256 x 256 tiles, no split-K
             if (!((c.variant == 0 && ((c.bn == 256 && (c.stages == 4 || c.stages == 3)) ||
-                                      (c.bn == 128 && (c.stages == 6 || c.stages == 4)))) ||
+                                      (c.bn == 128 && (c.stages == 6 || c.stages == 4)) ||
+                                      (c.bn == 512 && c.stages == 2))) ||
                   (c.variant == 1 && ((c.bn == 256 && c.stages == 3) ||
                                       (c.bn == 128 && c.stages == 4))) ||
                   (c.variant == 2 && c.bn == 256 && (c.stages == 6 || c.stages == 4))))
                 return GEMM_ERR_UNSUPPORTED;
             if (c.variant == 2 && c.split_k > 1) return GEMM_ERR_UNSUPPORTED;
+            // 512-wide tiles exist for the row softmax; the softmax needs the whole
+            // row in one tile with one epilogue thread per row
+            if (c.bn == 512 && p.epi.act != GEMM_ACT_SOFTMAX) return GEMM_ERR_UNSUPPORTED;
+            if (p.epi.act == GEMM_ACT_SOFTMAX &&
+                (c.variant != 0 || c.split_k > 1 || c.bn < p.N))
+                return GEMM_ERR_UNSUPPORTED;
             if (c.raster_group == 0) c.raster_group = 16;
             break;
         default:

@@ -143,7 +143,11 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                    const TcArgs args) {
     using L = TcLayout<BN, PAIR, K3>;
     static_assert(!(K3 && B_KN), "3xTF32 reads B K-major (the split pass transposes KN)");
-    constexpr uint32_t TMEM_COLS = 2 * BN;  // 256 or 512: powers of two
+    // Accumulator buffers in TMEM: two of BN columns, or one for 512-wide
+    // tiles (the row softmax), which fill all 512 columns.
+    constexpr int NBUF = BN > 256 ? 1 : 2;
+    constexpr uint32_t TMEM_COLS = NBUF * BN;  // 256 or 512: powers of two
+    constexpr int NHALF = BN > 256 ? 2 : 1;    // MMAs per K step (N <= 256 per MMA)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -249,7 +253,12 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                             for (int j = 0; j < L::B_ROWS / 64; ++j)
                                 load(smem_u32(sb + j * (64 * 128)), &tmB, n0 + 64 * j, kb * L::KE, bb);
                         } else {
-                            load(smem_u32(sb), &tmB, kb * L::KE, n0, bb);
+                            // K-major boxes of at most 256 rows (a TMA box limit)
+                            constexpr int BOXR = L::B_ROWS < 256 ? L::B_ROWS : 256;
+#pragma unroll
+                            for (int h = 0; h < L::B_ROWS / BOXR; ++h)
+                                load(smem_u32(sb + h * BOXR * 128), &tmB, kb * L::KE, n0 + h * BOXR,
+                                     bb);
                         }
                         armed |= 1u << s;
                         armed_par = (armed_par & ~(1u << s)) | (ph << s);
@@ -288,8 +297,8 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
             bool issued_any = false;
             int lt = 0;
             for (int64_t t = first_item; ok && t < args.total_items; t += item_stride, ++lt) {
-                const int buf = lt & 1;
-                const uint32_t tph = static_cast<uint32_t>(lt >> 1) & 1u;
+                const int buf = NBUF == 1 ? 0 : (lt & 1);
+                const uint32_t tph = static_cast<uint32_t>(NBUF == 1 ? lt : (lt >> 1)) & 1u;
                 if (!mbar_wait_bounded(smem_u32(&tempty[buf]), tph ^ 1u, abort_flag, args.status,
                                        tmo)) {
                     ok = false;
@@ -344,10 +353,16 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                             bdesc = smem_desc_sw128(sb + kk * 32, 16, 1024);
                         }
                         const uint32_t acc = ((kb - kb_lo) | kk) != 0 ? 1u : 0u;
-                        if (PAIR)
+                        if (PAIR) {
                             tc_mma_f16_pair(d_tmem, adesc, bdesc, args.idesc, acc);
-                        else
-                            tc_mma_f16(d_tmem, adesc, bdesc, args.idesc, acc);
+                        } else {
+                            // 512-wide tiles: two N = 256 MMAs, the second on B rows
+                            // (KN: panels) 256.. at +32 KB and accumulator columns 256..
+#pragma unroll
+                            for (int h = 0; h < NHALF; ++h)
+                                tc_mma_f16(d_tmem + h * 256, adesc, bdesc + h * (32768 >> 4),
+                                           args.idesc, acc);
+                        }
                     }
                     issued_any = true;
                     // stage s (in both CTAs of a pair) is free once these MMAs finish
@@ -402,8 +417,8 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
         bool ok = true;
         int lt = 0;
         for (int64_t t = first_item; ok && t < args.total_items; t += item_stride, ++lt) {
-            const int buf = lt & 1;
-            const uint32_t tph = static_cast<uint32_t>(lt >> 1) & 1u;
+            const int buf = NBUF == 1 ? 0 : (lt & 1);
+            const uint32_t tph = static_cast<uint32_t>(NBUF == 1 ? lt : (lt >> 1)) & 1u;
             if (!mbar_wait_bounded(smem_u32(&tfull[buf]), tph, abort_flag, args.status, tmo)) break;
             tc_fence_after();
             const int split = static_cast<int>(t / args.total_tiles);
@@ -415,6 +430,50 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
             const int64_t row = row0 + lane;
             const int64_t col0 = nt * BN;
             const uint32_t tbase = tmem_base + lane_base + static_cast<uint32_t>(buf * BN);
+            // Row softmax: this thread's row is all in TMEM (one tile spans N).
+            // Pass 1 finds the row maximum of t = alpha*acc + bias; pass 2
+            // overwrites each accumulator with e = exp(t - max) (zero past N)
+            // and sums them; the store loop below writes e / sum.  __expf
+            // (relative error ~1e-6 on [-88, 0]) keeps this one MUFU op per
+            // element.
+            float sinv = 0.0f;
+            if (e.act == GEMM_ACT_SOFTMAX) {
+                float m = -INFINITY;
+#pragma unroll 1
+                for (int c = 0; c < SLICE; c += 32) {
+                    if (col0 + c >= e.N) break;
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tbase + c, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int64_t col = col0 + c + i;
+                        float t = __uint_as_float(v[i]) * e.alpha;
+                        if (e.bias && col < e.N) t += __ldg(e.bias + col);
+                        if (col < e.N) m = fmaxf(m, t);
+                    }
+                }
+                float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 1
+                for (int c = 0; c < SLICE; c += 32) {
+                    if (col0 + c >= e.N) break;
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tbase + c, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int64_t col = col0 + c + i;
+                        float t = __uint_as_float(v[i]) * e.alpha;
+                        if (e.bias && col < e.N) t += __ldg(e.bias + col);
+                        const float ex = col < e.N ? __expf(t - m) : 0.0f;
+                        z[i & 3] += ex;
+                        v[i] = __float_as_uint(ex);
+                    }
+                    tmem_st_32x32b_x32(tbase + c, v);
+                }
+                tmem_st_wait();
+                sinv = 1.0f / ((z[0] + z[1]) + (z[2] + z[3]));
+            }
             if (args.epi_tma) {
                 const int W = args.out16 ? 64 : 32;  // columns per 128-byte chunk
 #pragma unroll 1
@@ -445,10 +504,11 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                                     static_cast<int32_t>(bt * args.r_bmul));
                     }
                     float y[64];
+                    const bool smx = e.act == GEMM_ACT_SOFTMAX;  // v holds exp(t - max)
 #pragma unroll
                     for (int i = 0; i < 64; ++i)
-                        if (i < W) y[i] = __uint_as_float(v[i]) * e.alpha;
-                    if (e.bias) {
+                        if (i < W) y[i] = __uint_as_float(v[i]) * (smx ? sinv : e.alpha);
+                    if (e.bias && !smx) {
                         const float* bp = e.bias + cg;
                         if (args.bias_vec && cg + W <= e.N) {
 #pragma unroll
@@ -569,7 +629,20 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                         // All of this buffer is in registers: hand it back to the MMA warp.
                         release(buf);
                     }
-                    if (col0 + c * 32 < e.N) {
+                    if (col0 + c * 32 < e.N && e.act == GEMM_ACT_SOFTMAX) {
+                        // the probabilities, then a plain store (cast only)
+                        EpiParams ep = e;
+                        ep.alpha = 1.0f;
+                        ep.bias = nullptr;
+                        ep.act = GEMM_ACT_NONE;
+                        float pr[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) pr[i] = __uint_as_float(r[i]) * sinv;
+#pragma unroll
+                        for (int g = 0; g < 8; ++g)
+                            epi_store4(ep, b, row, col0 + c * 32 + 4 * g, pr[4 * g], pr[4 * g + 1],
+                                       pr[4 * g + 2], pr[4 * g + 3]);
+                    } else if (col0 + c * 32 < e.N) {
 #pragma unroll
                         for (int g = 0; g < 8; ++g)
                             epi_store4(e, b, row, col0 + c * 32 + 4 * g, __uint_as_float(r[4 * g]),
@@ -634,7 +707,7 @@ cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& 
     // 17-22; M >> 4 at bits 24-28.
     const uint32_t ab = K3 ? 2u : dtype == GEMM_BF16 ? 1u : 0u;
     a.idesc = (1u << 4) | (ab << 7) | (ab << 10) | ((B_KN ? 1u : 0u) << 16) |
-              (static_cast<uint32_t>(BN >> 3) << 17) |
+              (static_cast<uint32_t>((BN > 256 ? 256 : BN) >> 3) << 17) |
               (static_cast<uint32_t>(L::TILE_M >> 4) << 24);
     a.e = e;
     a.status = lc.status;
@@ -702,6 +775,7 @@ cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& 
     X(128, 4, 4, 0, false)   \
     X(256, 3, 8, 1, false)   \
     X(128, 4, 8, 1, false)   \
+    X(512, 2, 4, 0, false)   \
     X(256, 6, 4, 2, true)    \
     X(256, 4, 4, 2, true)
 

@@ -126,6 +126,12 @@ def _qkt(dt):
                     note="96 heads of Q[512,64] K[512,64]^T / 8")
 
 
+def _qkt_softmax(dt):
+    return Workload(f"qkt_softmax_{dt}", dt, 512, 512, 64, batch=96, b_layout="nk", alpha=0.125,
+                    act="softmax", out_dtype="bf16",
+                    note="96 heads of softmax(Q[512,64] K[512,64]^T / 8) by rows, BF16 out")
+
+
 WORKLOADS = {w.name: w for w in [
     Workload("sgemm_256", "f32", 256, 256, 256, dist_a="uniform", dist_b="uniform",
              note="FP32 256^3, U[-1,1], seed 0"),
@@ -135,6 +141,7 @@ WORKLOADS = {w.name: w for w in [
     Workload("bf16_8192", "bf16", 8192, 8192, 8192, b_layout="nk",
              note="BF16 8192^3, K-major B, FP32 out"),
     _ffn1("bf16"), _ffn1("f16"), _ffn2("bf16"), _ffn2("f16"), _qkt("bf16"), _qkt("f16"),
+    _qkt_softmax("bf16"), _qkt_softmax("f16"),
 ]}
 
 SWEEP_SIZES = (1, 17, 127, 1000, 3001, 4097, 6144)

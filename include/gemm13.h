@@ -46,7 +46,12 @@ typedef enum { GEMM_F32 = 0, GEMM_F16 = 1, GEMM_BF16 = 2 } gemm_dtype_t;
 typedef enum {
     GEMM_ACT_NONE = 0,
     GEMM_ACT_GELU_ERF = 1, /* 0.5*y*(1+erf(y/sqrt(2))) */
-    GEMM_ACT_RELU = 2      /* max(y, 0) */
+    GEMM_ACT_RELU = 2,     /* max(y, 0) */
+    GEMM_ACT_SOFTMAX = 3   /* softmax over each output row: exp(y_ij - max_j y_ij) divided by
+                              sum_j exp(y_ij - max_j y_ij), with y = alpha*A.B + bias over all N
+                              columns -- the attention step Softmax(QK^T) of "CUDA Tile ...
+                              GEMM", sec. 2, fused into the GEMM.  16-bit inputs, N <= 512,
+                              K >= 1, no residual (else GEMM_ERR_UNSUPPORTED). */
 } gemm_act_t;
 
 typedef enum {
@@ -85,7 +90,7 @@ typedef struct {
     gemm_blayout_t b_layout; /* default GEMM_B_KN */
     gemm_dtype_t out_dtype;  /* GEMM_F32 (default), GEMM_BF16 or GEMM_F16; RNE cast */
     int has_bias;            /* 1: bias[N] FP32 added after the alpha scale */
-    gemm_act_t act;          /* applied after bias, before the residual */
+    gemm_act_t act;          /* applied after bias, before the residual (softmax: per row) */
     int has_residual;        /* 1: beta * R[M,N] (FP32, row-major, ldr) added last */
     float beta;              /* residual scale, default 1 */
     int64_t ldr;             /* residual leading dimension; 0 means ldc */

@@ -325,9 +325,50 @@ def test_batched_residual_tma(batch_r):
 
 
 # ---------------------------------------------------------------- named workloads
-@pytest.mark.parametrize("name", ["sgemm_256", "qkt_bf16", "qkt_f16"])
+@pytest.mark.parametrize("name", ["sgemm_256", "qkt_bf16", "qkt_f16", "qkt_softmax_bf16",
+                                  "qkt_softmax_f16"])
 def test_workload_full(name):
     full_check(Run(WORKLOADS[name]))
+
+
+# ---------------------------------------------------------------- row softmax epilogue
+SOFTMAX_CASES = [
+    # (M, N, K, layout, bias, out, ldc_pad): N up to 256 runs 256-wide tiles with two TMEM
+    # buffers, above that 512-wide tiles (two N = 256 MMAs per K step, one buffer)
+    (300, 77, 64, "nk", False, "f32", 0),
+    (129, 256, 100, "nk", True, "bf16", 0),
+    (200, 257, 64, "kn", True, "f32", 0),
+    (513, 512, 72, "nk", False, "bf16", 0),
+    (64, 300, 200, "kn", True, "f16", 0),
+    (1, 1, 16, "nk", False, "f32", 0),        # a single column: p = 1
+    (77, 500, 64, "nk", True, "f32", 1),      # odd ldc: per-thread stores
+    (3, 129, 1500, "kn", True, "bf16", 1),
+]
+
+
+@pytest.mark.parametrize("case", SOFTMAX_CASES, ids=lambda c: "x".join(map(str, c[:3])) + c[3])
+def test_softmax_rows(case):
+    M, N, K, layout, bias, out, pad = case
+    w = Workload("softmax_" + "x".join(map(str, case[:3])), "bf16", M, N, K, b_layout=layout,
+                 alpha=0.125, bias=bias, act="softmax", out_dtype=out)
+    run = Run(w, ldc_pad=pad)
+    cfg = run.info["config"]
+    assert (cfg.kernel, cfg.bn, cfg.split_k) == ("tc", 256 if N <= 256 else 512, 1)
+    C = full_check(run)
+    if out == "f32":
+        assert np.all(np.abs(C.sum(axis=-1) - 1.0) <= 1e-5)     # each row sums to one
+    # persistent grid smaller than the tile count
+    cfg2 = g13.Config("tc", 128, cfg.bn, 64, cfg.stages, num_ctas=3)
+    assert np.array_equal(Run(w, tensors=run.t, config=cfg2, ldc_pad=pad).run().result(), C)
+
+
+def test_softmax_batched_large_logits():
+    # 8 heads, alpha = 2 on N(0,1) BF16 inputs with K = 256: logits of size ~30,
+    # exp would overflow without the row maximum
+    w = Workload("softmax_big", "f16", 256, 384, 256, batch=8, b_layout="nk", alpha=2.0,
+                 act="softmax", out_dtype="f32")
+    C = full_check(Run(w))
+    assert np.all(np.isfinite(C)) and np.all(np.abs(C.sum(axis=-1) - 1.0) <= 1e-5)
 
 
 @pytest.mark.parametrize("name", ["sgemm_4096", "bf16_4096", "bf16_8192", "ffn1_bf16", "ffn1_f16",
