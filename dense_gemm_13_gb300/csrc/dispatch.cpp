@@ -176,13 +176,14 @@ int choose_config(const Problem& p, int num_sms, gemm_config_t* out) {
     const int64_t M = p.M, N = p.N, K = p.K, bt = p.epi.batch;
     if (p.epi.act == GEMM_ACT_SOFTMAX && M > 0 && N > 0) {
         // one tile spans the whole row: 256 columns (double-buffered TMEM) or
-        // 512 (single-buffered); 4 epilogue warps, one thread per row
+        // 512 (single-buffered, one 80 KB stage); 8 epilogue warps, two per
+        // TMEM lane quarter, each thread half a row
         c.kernel = GEMM_KERNEL_TC;
         c.bm = 128;
         c.bk = 64;
         c.bn = N <= 256 ? 256 : 512;
-        c.stages = N <= 256 ? 4 : 2;
-        c.variant = 0;
+        c.stages = N <= 256 ? 3 : 1;
+        c.variant = 1;
         c.raster_group = static_cast<int32_t>(std::min<int64_t>(16, cdiv(M, 128)));
         set_staging(p, &c);
         *out = c;
@@ -326,10 +327,10 @@ int check_config(const Problem& p, const gemm_config_t& in, gemm_config_t* out) 
             // (BN, stages) pairs with 4 epilogue warps (variant 0) or 8 (variant 1);
             // variant 2: CTA pairs on 256 x 256 tiles, no split-K
             if (!((c.variant == 0 && ((c.bn == 256 && (c.stages == 4 || c.stages == 3)) ||
-                                      (c.bn == 128 && (c.stages == 6 || c.stages == 4)) ||
-                                      (c.bn == 512 && c.stages == 2))) ||
+                                      (c.bn == 128 && (c.stages == 6 || c.stages == 4)))) ||
                   (c.variant == 1 && ((c.bn == 256 && c.stages == 3) ||
-                                      (c.bn == 128 && c.stages == 4))) ||
+                                      (c.bn == 128 && c.stages == 4) ||
+                                      (c.bn == 512 && c.stages == 1))) ||
                   (c.variant == 2 && c.bn == 256 && (c.stages == 6 || c.stages == 4))))
                 return GEMM_ERR_UNSUPPORTED;
             if (c.variant == 2 && c.split_k > 1) return GEMM_ERR_UNSUPPORTED;
@@ -337,7 +338,7 @@ int check_config(const Problem& p, const gemm_config_t& in, gemm_config_t* out) 
             // row in one tile with one epilogue thread per row
             if (c.bn == 512 && p.epi.act != GEMM_ACT_SOFTMAX) return GEMM_ERR_UNSUPPORTED;
             if (p.epi.act == GEMM_ACT_SOFTMAX &&
-                (c.variant != 0 || c.split_k > 1 || c.bn < p.N))
+                (c.variant == TC_VARIANT_PAIR || c.split_k > 1 || c.bn < p.N))
                 return GEMM_ERR_UNSUPPORTED;
             if (c.raster_group == 0) c.raster_group = 16;
             break;

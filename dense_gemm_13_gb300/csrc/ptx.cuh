@@ -290,6 +290,14 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
         : "memory");
 }
 
+// 2^x, the MUFU approximation (relative error ~2^-22; results below 2^-126
+// flush to zero).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // The inverse of tmem_ld_32x32b_x32: thread t of the warp writes columns
 // [col, col+32) of TMEM lane (lane_base + t).
 __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {

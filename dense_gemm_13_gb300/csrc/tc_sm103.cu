@@ -113,8 +113,10 @@ __host__ __device__ constexpr int tc_bar_off() {
 template <int BN, int STAGES, int EW, bool PAIR, bool K3>
 __host__ __device__ constexpr int tc_smem_total() {
     // ring + epilogue tiles + full/empty per stage + tfull/tempty x2 + drain
-    // + residual barriers (2 per epilogue warp) + tmem slot + abort flag
-    return 1024 + tc_bar_off<BN, STAGES, EW, PAIR, K3>() + (2 * STAGES + 5 + 2 * EW) * 8 + 16;
+    // + residual barriers (2 per epilogue warp) + softmax exchange barriers (4)
+    // + tmem slot + abort flag + softmax exchange values [2][EW][32] floats
+    return 1024 + tc_bar_off<BN, STAGES, EW, PAIR, K3>() + (2 * STAGES + 9 + 2 * EW) * 8 + 16 +
+           2 * EW * 32 * 4;
 }
 
 __device__ __forceinline__ void tc_tile_coords(int64_t t, const TcArgs& a, int64_t& b, int64_t& mt,
@@ -157,8 +159,10 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
     uint64_t* rbar = drain + 1;  // [EW][2] residual-chunk barriers
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rbar + 2 * EW);
+    uint64_t* xbar = rbar + 2 * EW;  // [4] softmax: the two warps of a lane quarter meet
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 4);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(tmem_slot + 1);
+    float* xch = reinterpret_cast<float*>(tmem_slot + 4);  // [2][EW][32] softmax partials
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Pair mode: rank 0 / 1 in the CTA pair; the pair walks tiles together.
@@ -178,6 +182,7 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
         }
         mbar_init(smem_u32(drain), 1);
         for (int i = 0; i < 2 * EW; ++i) mbar_init(smem_u32(&rbar[i]), 1);
+        for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&xbar[i]), 64);
         *abort_flag = 0u;
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
@@ -430,49 +435,99 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
             const int64_t row = row0 + lane;
             const int64_t col0 = nt * BN;
             const uint32_t tbase = tmem_base + lane_base + static_cast<uint32_t>(buf * BN);
-            // Row softmax: this thread's row is all in TMEM (one tile spans N).
-            // Pass 1 finds the row maximum of t = alpha*acc + bias; pass 2
-            // overwrites each accumulator with e = exp(t - max) (zero past N)
-            // and sums them; the store loop below writes e / sum.  __expf
-            // (relative error ~1e-6 on [-88, 0]) keeps this one MUFU op per
-            // element.
+            // Row softmax: this thread's row is all in TMEM (one tile spans N);
+            // with 8 epilogue warps the row's columns are split between the
+            // two warps of a lane quarter, which trade their partial maximum
+            // and sum through shared memory (both arrive on xbar[q], bounded
+            // wait; two phases per tile, so exchange k waits on parity k).
+            // Work in the base-2 domain, u = t * log2(e) with t = alpha*acc +
+            // bias: pass 1 finds the maximum m of u over the row; pass 2
+            // overwrites each accumulator with 2^(u - m) (ex2.approx, one MUFU
+            // op) and sums them; the store loop below writes each value
+            // divided by the sum.  Columns past N are skipped (only the last
+            // chunk checks).
             float sinv = 0.0f;
-            if (e.act == GEMM_ACT_SOFTMAX) {
-                float m = -INFINITY;
-#pragma unroll 1
-                for (int c = 0; c < SLICE; c += 32) {
-                    if (col0 + c >= e.N) break;
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(tbase + c, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int64_t col = col0 + c + i;
-                        float t = __uint_as_float(v[i]) * e.alpha;
-                        if (e.bias && col < e.N) t += __ldg(e.bias + col);
-                        if (col < e.N) m = fmaxf(m, t);
-                    }
+            bool xok = true;
+            const auto exchange = [&](int k, float val) {
+                if (EW != 8) return val;
+                float* xb = xch + k * EW * 32;
+                xb[ew * 32 + lane] = val;
+                mbar_arrive(smem_u32(&xbar[q]));
+                if (!mbar_wait_bounded(smem_u32(&xbar[q]), static_cast<uint32_t>(k), abort_flag,
+                                       args.status, tmo)) {
+                    xok = false;
+                    return val;
                 }
+                return xb[(ew ^ 4) * 32 + lane];
+            };
+            if (e.act == GEMM_ACT_SOFTMAX) {
+                constexpr float LOG2E = 1.4426950408889634f;
+                const float a2 = e.alpha * LOG2E;
+                // valid columns in this warp's slice (int32: at most SLICE)
+                const int nrow = static_cast<int>(
+                    max(static_cast<int64_t>(0),
+                        min(static_cast<int64_t>(SLICE), e.N - (col0 + c_lo))));
+                const float* bias = e.bias ? e.bias + col0 + c_lo : nullptr;
+                float mu = -INFINITY;  // max over the slice of u
+#pragma unroll 1
+                for (int c = 0; c < nrow; c += 32) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tbase + c_lo + c, v);
+                    tmem_ld_wait();
+                    const int nv = min(32, nrow - c);
+                    float mc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                    if (nv == 32 && !bias) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            mc[i & 3] = fmaxf(mc[i & 3], __uint_as_float(v[i]) * a2);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (i < nv) {
+                                const float ub = bias ? __ldg(bias + c + i) * LOG2E : 0.0f;
+                                mc[i & 3] = fmaxf(mc[i & 3], fmaf(__uint_as_float(v[i]), a2, ub));
+                            }
+                    }
+                    mu = fmaxf(mu, fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])));
+                }
+                mu = fmaxf(mu, exchange(0, mu));
                 float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll 1
-                for (int c = 0; c < SLICE; c += 32) {
-                    if (col0 + c >= e.N) break;
+                for (int c = 0; c < nrow; c += 32) {
                     uint32_t v[32];
-                    tmem_ld_32x32b_x32(tbase + c, v);
+                    tmem_ld_32x32b_x32(tbase + c_lo + c, v);
                     tmem_ld_wait();
+                    const int nv = min(32, nrow - c);
+                    if (nv == 32 && !bias) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int64_t col = col0 + c + i;
-                        float t = __uint_as_float(v[i]) * e.alpha;
-                        if (e.bias && col < e.N) t += __ldg(e.bias + col);
-                        const float ex = col < e.N ? __expf(t - m) : 0.0f;
-                        z[i & 3] += ex;
-                        v[i] = __float_as_uint(ex);
+                        for (int i = 0; i < 32; ++i) {
+                            const float ex = ex2_approx(fmaf(__uint_as_float(v[i]), a2, -mu));
+                            z[i & 3] += ex;
+                            v[i] = __float_as_uint(ex);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            float ex = 0.0f;
+                            if (i < nv) {
+                                const float ub = bias ? fmaf(__ldg(bias + c + i), LOG2E, -mu) : -mu;
+                                ex = ex2_approx(fmaf(__uint_as_float(v[i]), a2, ub));
+                            }
+                            z[i & 3] += ex;
+                            v[i] = __float_as_uint(ex);
+                        }
                     }
-                    tmem_st_32x32b_x32(tbase + c, v);
+                    tmem_st_32x32b_x32(tbase + c_lo + c, v);
                 }
                 tmem_st_wait();
-                sinv = 1.0f / ((z[0] + z[1]) + (z[2] + z[3]));
+                const float zh = (z[0] + z[1]) + (z[2] + z[3]);
+                const float zp = exchange(1, zh);
+                // the same order in both warps: lower column half first
+                sinv = 1.0f / (EW == 8 ? (ew < 4 ? zh + zp : zp + zh) : zh);
+                if (!xok) {
+                    ok = false;
+                    break;
+                }
             }
             if (args.epi_tma) {
                 const int W = args.out16 ? 64 : 32;  // columns per 128-byte chunk
@@ -775,7 +830,7 @@ cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& 
     X(128, 4, 4, 0, false)   \
     X(256, 3, 8, 1, false)   \
     X(128, 4, 8, 1, false)   \
-    X(512, 2, 4, 0, false)   \
+    X(512, 1, 8, 1, false)   \
     X(256, 6, 4, 2, true)    \
     X(256, 4, 4, 2, true)
 

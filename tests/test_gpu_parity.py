@@ -358,8 +358,12 @@ def test_softmax_rows(case):
     if out == "f32":
         assert np.all(np.abs(C.sum(axis=-1) - 1.0) <= 1e-5)     # each row sums to one
     # persistent grid smaller than the tile count
-    cfg2 = g13.Config("tc", 128, cfg.bn, 64, cfg.stages, num_ctas=3)
+    cfg2 = g13.Config("tc", 128, cfg.bn, 64, cfg.stages, num_ctas=3, variant=cfg.variant)
     assert np.array_equal(Run(w, tensors=run.t, config=cfg2, ldc_pad=pad).run().result(), C)
+    if N <= 256:
+        # one thread per whole row (4 epilogue warps, no exchange between warps)
+        cfg4 = g13.Config("tc", 128, 256, 64, 4)
+        full_check(Run(w, tensors=run.t, config=cfg4, ldc_pad=pad))
 
 
 def test_softmax_batched_large_logits():

@@ -141,9 +141,9 @@ def test_dispatch_buckets(lib):
 def test_softmax_limits(lib):
     # the row softmax: tensor cores, one tile per row, 16-bit inputs only
     c = sel("bf16", 512, 512, 64, "nk", act="softmax")
-    assert (c.kernel, c.bn, c.stages, c.variant, c.split_k) == ("tc", 512, 2, 0, 1)
+    assert (c.kernel, c.bn, c.stages, c.variant, c.split_k) == ("tc", 512, 1, 1, 1)
     c = sel("bf16", 4, 200, 4096, "nk", act="softmax")     # small M: still the tile kernel
-    assert (c.kernel, c.bn) == ("tc", 256)
+    assert (c.kernel, c.bn, c.stages, c.variant) == ("tc", 256, 3, 1)
     for kw in (dict(dtype="f32"), dict(N=513), dict(K=0), dict(residual=True)):
         args = dict(dtype="bf16", M=64, N=300, K=64)
         args.update({k: v for k, v in kw.items() if k in ("dtype", "N", "K")})
@@ -151,9 +151,7 @@ def test_softmax_limits(lib):
             sel(args["dtype"], args["M"], args["N"], args["K"], "nk", act="softmax",
                 residual=kw.get("residual", False))
         assert ei.value.status == -2, kw
-    with pytest.raises(g13.GemmError):     # a forced 8-warp epilogue cannot hold a row per thread
-        g13.gemm_plan("bf16", 64, 300, 64, 64, 64, 300, g13.Epilogue(b_layout="nk", act="softmax"),
-                      g13.Config("tc", 128, 256, 64, 3, variant=1))
+
 
 
 def test_dispatch_staging_follows_alignment(lib):
