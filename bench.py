@@ -94,7 +94,8 @@ def peaks():
             "sm_max_mhz": 2070.0}, "fallback"
 
 
-KERNEL_SOURCES = {"tc": "tc_sm103.cu", "ffma": "sgemm_ffma.cu", "skinny": "aux_kernels.cu"}
+KERNEL_SOURCES = {"tc": "tc_sm103.cu", "ffma": "sgemm_ffma.cu", "skinny": "aux_kernels.cu",
+                  "tf32x3": "tc_sm103.cu"}
 
 
 def source_hash(kernel: str) -> str:
@@ -399,9 +400,11 @@ def run_ours(args):
     g13.load()
     pk, pk_kind = peaks()
 
-    w = WORKLOADS[args.workload]
+    # "<workload>+3xtf32": the same FP32 workload with GEMM_FLAG_FP32_TENSOR
+    base, _, mode = args.workload.partition("+")
+    w = WORKLOADS[base]
     host, dev = make_device_inputs(w, 0, device)
-    plan = make_plan(g13, w)
+    plan = make_plan(g13, w, g13.FLAG_FP32_TENSOR if mode == "3xtf32" else 0)
     info = plan.info()
     kernel = info["config"].kernel
     odt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[w.out_dtype]
@@ -419,7 +422,7 @@ def run_ours(args):
         "value": round(value, 3), "unit": "TFLOPS", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(med, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "batch": w.batch,
+        "config": {"workload": args.workload, "M": w.M, "N": w.N, "K": w.K, "batch": w.batch,
                    "b_layout": w.b_layout, "out_dtype": w.out_dtype, "epilogue": {
                        "alpha": w.alpha, "bias": w.bias, "act": w.act, "residual": w.residual,
                        "beta": w.beta},
@@ -484,7 +487,7 @@ def run_reference(args):
     import numpy as np
     import oracle
     from dense_gemm_13_gb300.inputs import WORKLOADS, host_view
-    w = WORKLOADS[args.workload]
+    w = WORKLOADS[args.workload.partition("+")[0]]
     host = w.make(0)
     A, B = host_view(host["A"]), host_view(host["B"])
     bias = host["bias"].numpy() if host["bias"] is not None else None
@@ -514,7 +517,7 @@ def run_reference(args):
            "dtype roofline", "value": round(val, 6), "unit": "TFLOPS", "n_gpus": args.gpus,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(med * 1e3, 3),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-           "data": "synthetic", "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+           "data": "synthetic", "config": {"workload": args.workload, "M": w.M, "N": w.N, "K": w.K,
                                            "batch": w.batch},
            "cpu_baseline": {"value": round(val, 6), "unit": "TFLOPS", "cores": threads,
                             "kind": "oracle",
