@@ -108,9 +108,9 @@ def source_hash(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, workload: str):
+def recorded_traffic(kernel: str, workload: str, root: str = ROOT):
     """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged since."""
-    path = os.path.join(ROOT, "profiles", f"ncu_{kernel}_{workload}.md")
+    path = os.path.join(root, "profiles", f"ncu_{kernel}_{workload}.md")
     if not os.path.exists(path) or kernel not in KERNEL_SOURCES:
         return None
     txt = open(path).read()
