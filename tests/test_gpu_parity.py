@@ -331,6 +331,23 @@ def test_workload_full(name):
     full_check(Run(WORKLOADS[name]))
 
 
+def test_tc_gelu_pointwise():
+    # K = 1 and B = 1 turn the GEMM into GELU(x) on 256 x values in [-8, 8] (exact BF16):
+    # the tensor-core epilogue's erf (Abramowitz & Stegun 7.1.26, |error| <= 1.5e-7) must
+    # stay within 4e-7 * max(1, |x|) of the FP64 erf form, far inside the GEMM tolerance
+    xs = torch.linspace(-8.0, 8.0, 256, dtype=torch.float64).to(torch.bfloat16)
+    A = xs.reshape(256, 1).contiguous()
+    B = torch.ones((256, 1), dtype=torch.bfloat16)          # NK: B[n][k]
+    w = Workload("gelu_points", "bf16", 256, 256, 1, b_layout="nk", act="gelu")
+    run = Run(w, tensors={"A": A, "B": B, "bias": None, "R": None})
+    assert run.info["config"].kernel == "tc"
+    C = run.run().result()
+    _, cref, _ = run.oracle()
+    x = xs.double().numpy()[:, None]
+    assert np.all(np.abs(C - cref.reshape(C.shape)) <= 4e-7 * np.maximum(1.0, np.abs(x)))
+    run.check(C)
+
+
 # ---------------------------------------------------------------- row softmax epilogue
 SOFTMAX_CASES = [
     # (M, N, K, layout, bias, out, ldc_pad): N up to 256 runs 256-wide tiles with two TMEM
