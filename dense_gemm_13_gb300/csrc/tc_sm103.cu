@@ -107,6 +107,7 @@ struct TcArgs {
     int kb_per_split;
     int64_t total_items;  // total_tiles * splits (split-major order)
     int bias_vec;   // 1: bias is 16-byte aligned (float4 loads)
+    int epi_plain;  // 1: no bias, activation or residual (C = alpha * acc, cast)
     int64_t n_tma;  // columns [0, n_tma) go out by TMA (a multiple of 16 bytes); the rest,
                     // fewer than 16 bytes per row, from registers
     int64_t m_tiles, n_tiles, tiles_per_batch, total_tiles;
@@ -142,15 +143,20 @@ __host__ __device__ constexpr int tc_smem_total() {
            2 * EW * 32 * 4;
 }
 
+// 32-bit arithmetic: the host keeps the tile count below 2^31.
 __device__ __forceinline__ void tc_tile_coords(int64_t t, const TcArgs& a, int64_t& b, int64_t& mt,
                                                int64_t& nt) {
-    b = t / a.tiles_per_batch;
-    const int64_t r = t - b * a.tiles_per_batch;
-    const int64_t span = static_cast<int64_t>(a.raster) * a.n_tiles;
-    const int64_t g = r / span;
-    const int64_t first = g * a.raster;
-    const int64_t gm = min(static_cast<int64_t>(a.raster), a.m_tiles - first);
-    const int64_t w = r - g * span;
+    const uint32_t tu = static_cast<uint32_t>(t);
+    const uint32_t tpb = static_cast<uint32_t>(a.tiles_per_batch);
+    const uint32_t bu = tu / tpb;
+    const uint32_t r = tu - bu * tpb;
+    const uint32_t span = static_cast<uint32_t>(a.raster) * static_cast<uint32_t>(a.n_tiles);
+    const uint32_t g = r / span;
+    const uint32_t first = g * static_cast<uint32_t>(a.raster);
+    const uint32_t gm =
+        min(static_cast<uint32_t>(a.raster), static_cast<uint32_t>(a.m_tiles) - first);
+    const uint32_t w = r - g * span;
+    b = bu;
     mt = first + w % gm;
     nt = w / gm;
 }
@@ -583,63 +589,72 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                     }
                     float y[64];
                     const bool smx = e.act == GEMM_ACT_SOFTMAX;  // v holds exp(t - max)
-#pragma unroll
-                    for (int i = 0; i < 64; ++i)
-                        if (i < W) y[i] = __uint_as_float(v[i]) * (smx ? sinv : e.alpha);
-                    if (e.bias && !smx) {
-                        const float* bp = e.bias + cg;
-                        if (args.bias_vec && cg + W <= e.N) {
-#pragma unroll
-                            for (int i = 0; i < 64; i += 4)
-                                if (i < W) {
-                                    const float4 bv = __ldg(reinterpret_cast<const float4*>(bp + i));
-                                    y[i] += bv.x;
-                                    y[i + 1] += bv.y;
-                                    y[i + 2] += bv.z;
-                                    y[i + 3] += bv.w;
-                                }
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 64; ++i)
-                                if (i < W && cg + i < e.N) y[i] += __ldg(bp + i);
-                        }
-                    }
-                    if (e.act == GEMM_ACT_GELU_ERF) {
-#pragma unroll
-                        for (int i = 0; i < 64; ++i)
-                            if (i < W) y[i] = gelu_as7126(y[i]);
-                    } else if (e.act == GEMM_ACT_RELU) {
-#pragma unroll
-                        for (int i = 0; i < 64; ++i)
-                            if (i < W) y[i] = fmaxf(y[i], 0.0f);
-                    }
                     // 16-byte chunk j of this thread's row sits at position j ^ (row & 7).
                     uint8_t* rowp = sb + lane * 128;
-                    if (e.R) {
-                        if (args.r_tma) {
-                            if (!mbar_wait_bounded(smem_u32(&rb[sel]), (rph >> sel) & 1u, abort_flag,
-                                                   args.status, tmo)) {
-                                tc_drain(smem_u32(&rb[sel]), (rph >> sel) & 1u, tmo);
-                                ok = false;
-                                break;
-                            }
-                            rph ^= 1u << sel;
+                    // The plain case (scale only) first and compact: the general
+                    // steps below are large unrolled blocks that it jumps over once.
+                    if (args.epi_plain || smx) {
+                        const float sc = smx ? sinv : e.alpha;
 #pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                const float4 r4 =
-                                    *reinterpret_cast<const float4*>(rowp + ((j ^ (lane & 7)) << 4));
-                                y[4 * j] += e.beta * r4.x;
-                                y[4 * j + 1] += e.beta * r4.y;
-                                y[4 * j + 2] += e.beta * r4.z;
-                                y[4 * j + 3] += e.beta * r4.w;
+                        for (int i = 0; i < 64; ++i)
+                            if (i < W) y[i] = __uint_as_float(v[i]) * sc;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 64; ++i)
+                            if (i < W) y[i] = __uint_as_float(v[i]) * e.alpha;
+                        if (e.bias) {
+                            const float* bp = e.bias + cg;
+                            if (args.bias_vec && cg + W <= e.N) {
+#pragma unroll
+                                for (int i = 0; i < 64; i += 4)
+                                    if (i < W) {
+                                        const float4 bv = __ldg(reinterpret_cast<const float4*>(bp + i));
+                                        y[i] += bv.x;
+                                        y[i + 1] += bv.y;
+                                        y[i + 2] += bv.z;
+                                        y[i + 3] += bv.w;
+                                    }
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 64; ++i)
+                                    if (i < W && cg + i < e.N) y[i] += __ldg(bp + i);
                             }
-                        } else if (row < e.M) {
-                            const float* rp = e.R + bt * e.stride_r + row * e.ldr + cg;
+                        }
+                        if (e.act == GEMM_ACT_GELU_ERF) {
 #pragma unroll
                             for (int i = 0; i < 64; ++i)
-                                if (i < W && cg + i < e.N) y[i] += e.beta * __ldg(rp + i);
+                                if (i < W) y[i] = gelu_as7126(y[i]);
+                        } else if (e.act == GEMM_ACT_RELU) {
+#pragma unroll
+                            for (int i = 0; i < 64; ++i)
+                                if (i < W) y[i] = fmaxf(y[i], 0.0f);
                         }
-                    }
+                        if (e.R) {
+                            if (args.r_tma) {
+                                if (!mbar_wait_bounded(smem_u32(&rb[sel]), (rph >> sel) & 1u, abort_flag,
+                                                       args.status, tmo)) {
+                                    tc_drain(smem_u32(&rb[sel]), (rph >> sel) & 1u, tmo);
+                                    ok = false;
+                                    break;
+                                }
+                                rph ^= 1u << sel;
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) {
+                                    const float4 r4 =
+                                        *reinterpret_cast<const float4*>(rowp + ((j ^ (lane & 7)) << 4));
+                                    y[4 * j] += e.beta * r4.x;
+                                    y[4 * j + 1] += e.beta * r4.y;
+                                    y[4 * j + 2] += e.beta * r4.z;
+                                    y[4 * j + 3] += e.beta * r4.w;
+                                }
+                            } else if (row < e.M) {
+                                const float* rp = e.R + bt * e.stride_r + row * e.ldr + cg;
+#pragma unroll
+                                for (int i = 0; i < 64; ++i)
+                                    if (i < W && cg + i < e.N) y[i] += e.beta * __ldg(rp + i);
+                            }
+                        }
+                    }  // general epilogue
                     if (!args.out16) {
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
@@ -769,6 +784,7 @@ cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& 
     a.c_smul = em ? em->c_smul : 0;
     a.r_bmul = em ? em->r_bmul : 0;
     a.bias_vec = e.bias && (reinterpret_cast<uintptr_t>(e.bias) % 16 == 0);
+    a.epi_plain = !e.bias && e.act == GEMM_ACT_NONE && !e.R;
     a.n_tma = em ? em->n_tma : 0;
     a.m_tiles = (s.M + L::TILE_M - 1) / L::TILE_M;
     a.n_tiles = (s.N + BN - 1) / BN;
@@ -778,6 +794,7 @@ cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& 
     a.splits = (PAIR || K3) ? 1 : tc_effective_splits(s.K, cfg.split_k);
     a.kb_per_split = (a.k_blocks + a.splits - 1) / a.splits;
     a.total_items = a.total_tiles * a.splits;
+    if (a.total_items >= (int64_t(1) << 31)) return cudaErrorInvalidValue;  // 32-bit tile coordinates
     a.raster = cfg.raster_group > 0 ? cfg.raster_group : 16;
     // Instruction descriptor, kind::f16 / kind::tf32: D = F32 (bits 4-5 = 1);
     // A and B type (bits 7-9, 10-12) 0 = F16, 1 = BF16, 2 = TF32; A K-major
