@@ -44,6 +44,7 @@
 // Every wait is bounded (ptx.cuh); on a timeout the CTA drains its own copies
 // and MMAs, frees TMEM and exits, and the plan's status word records it.
 #include <atomic>
+#include <type_traits>
 
 #include "epilogue.cuh"
 #include "internal.h"
@@ -559,12 +560,17 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                 }
             }
             if (args.epi_tma) {
-                const int W = args.out16 ? 64 : 32;  // columns per 128-byte chunk
+                // The chunk loop, compiled for each chunk width (W columns = 128
+                // bytes: 32 FP32 or 64 16-bit) so its arrays are exactly W long
+                // (a runtime width kept 64 of each live and spilled).  Returns
+                // false when a residual wait gave up.
+                const auto chunk_loop = [&](auto w_tag) -> bool {
+                constexpr int W = decltype(w_tag)::value;
 #pragma unroll 1
                 for (int c = c_lo; c < c_lo + SLICE; c += W) {
-                    uint32_t v[64];
+                    uint32_t v[W];
                     tmem_ld_32x32b_x32(tbase + c, *reinterpret_cast<uint32_t(*)[32]>(v));
-                    if (W == 64)
+                    if constexpr (W == 64)
                         tmem_ld_32x32b_x32(tbase + c + 32,
                                            *reinterpret_cast<uint32_t(*)[32]>(v + 32));
                     tmem_ld_wait();
@@ -587,7 +593,7 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                                     static_cast<int32_t>(cg), row0,
                                     static_cast<int32_t>(bt * args.r_bmul));
                     }
-                    float y[64];
+                    float y[W];
                     const bool smx = e.act == GEMM_ACT_SOFTMAX;  // v holds exp(t - max)
                     // 16-byte chunk j of this thread's row sits at position j ^ (row & 7).
                     uint8_t* rowp = sb + lane * 128;
@@ -596,17 +602,17 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                     if (args.epi_plain || smx) {
                         const float sc = smx ? sinv : e.alpha;
 #pragma unroll
-                        for (int i = 0; i < 64; ++i)
+                        for (int i = 0; i < W; ++i)
                             if (i < W) y[i] = __uint_as_float(v[i]) * sc;
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 64; ++i)
+                        for (int i = 0; i < W; ++i)
                             if (i < W) y[i] = __uint_as_float(v[i]) * e.alpha;
                         if (e.bias) {
                             const float* bp = e.bias + cg;
                             if (args.bias_vec && cg + W <= e.N) {
 #pragma unroll
-                                for (int i = 0; i < 64; i += 4)
+                                for (int i = 0; i < W; i += 4)
                                     if (i < W) {
                                         const float4 bv = __ldg(reinterpret_cast<const float4*>(bp + i));
                                         y[i] += bv.x;
@@ -616,17 +622,17 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                                     }
                             } else {
 #pragma unroll
-                                for (int i = 0; i < 64; ++i)
+                                for (int i = 0; i < W; ++i)
                                     if (i < W && cg + i < e.N) y[i] += __ldg(bp + i);
                             }
                         }
                         if (e.act == GEMM_ACT_GELU_ERF) {
 #pragma unroll
-                            for (int i = 0; i < 64; ++i)
+                            for (int i = 0; i < W; ++i)
                                 if (i < W) y[i] = gelu_as7126(y[i]);
                         } else if (e.act == GEMM_ACT_RELU) {
 #pragma unroll
-                            for (int i = 0; i < 64; ++i)
+                            for (int i = 0; i < W; ++i)
                                 if (i < W) y[i] = fmaxf(y[i], 0.0f);
                         }
                         if (e.R) {
@@ -634,8 +640,7 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                                 if (!mbar_wait_bounded(smem_u32(&rb[sel]), (rph >> sel) & 1u, abort_flag,
                                                        args.status, tmo)) {
                                     tc_drain(smem_u32(&rb[sel]), (rph >> sel) & 1u, tmo);
-                                    ok = false;
-                                    break;
+                                    return false;
                                 }
                                 rph ^= 1u << sel;
 #pragma unroll
@@ -650,12 +655,12 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                             } else if (row < e.M) {
                                 const float* rp = e.R + bt * e.stride_r + row * e.ldr + cg;
 #pragma unroll
-                                for (int i = 0; i < 64; ++i)
+                                for (int i = 0; i < W; ++i)
                                     if (i < W && cg + i < e.N) y[i] += e.beta * __ldg(rp + i);
                             }
                         }
                     }  // general epilogue
-                    if (!args.out16) {
+                    if constexpr (W == 32) {  // FP32 out
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
                             *reinterpret_cast<float4*>(rowp + ((j ^ (lane & 7)) << 4)) =
@@ -711,6 +716,14 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                                         static_cast<uint16_t>(w[t >> 1] >> (16 * (t & 1)));
                         }
                     }
+                }
+                return true;
+                };
+                const bool cok = args.out16 ? chunk_loop(std::integral_constant<int, 64>{})
+                                            : chunk_loop(std::integral_constant<int, 32>{});
+                if (!cok) {
+                    ok = false;
+                    break;
                 }
             } else {
 #pragma unroll 1
