@@ -332,72 +332,66 @@ __global__ void __launch_bounds__(256, PMAX == 1 ? 3 : PMAX == 4 ? 2 : 1)
     }
 }
 
-// Adds the split partial sums and applies the epilogue.  With few splits each
-// thread owns one output and sums its splits in order (loads in flight four at
-// a time).  With many splits (> 16) a block covers 32 consecutive outputs: its 8
-// warps each sum an interleaved subset of the splits (warp w takes w, w+8, ...)
-// in order and warp 0 adds the 8 subtotals in warp order.  Both orders are
-// fixed, so results are run-to-run identical.
-__device__ __forceinline__ void reduce_store(const SkinnyParams& sp, int64_t i, float y) {
-    const int64_t b = i / (sp.P * sp.Q);
-    const int64_t pq = i - b * sp.P * sp.Q;
-    const int64_t p = pq / sp.Q, q = pq - p * sp.Q;
-    if (sp.p_is_m)
-        epi_store1(sp.e, b, p, q, y);
-    else
-        epi_store1(sp.e, b, q, p, y);
+// Split-K reduction for the tensor-core kernel: the partial slabs
+// [batch][split][M][N] (FP32, N contiguous) are added in split order and the
+// real epilogue is applied.  A thread owns four consecutive columns of one
+// row: 16-byte loads from each slab when N allows, 32-bit index arithmetic
+// when the quad count fits, and the vectorised four-column epilogue.
+__global__ void __launch_bounds__(256) split_reduce_kernel(const float* __restrict__ partial,
+                                                           int64_t M, int64_t N, int64_t batch,
+                                                           int splits, int vec, EpiParams e) {
+    const int64_t nq = (N + 3) / 4;
+    const int64_t total = batch * M * nq;
+    const int64_t slab = M * N;
+    const bool small = total < (int64_t(1) << 31);
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        int64_t r, qd;
+        if (small) {
+            const uint32_t iu = static_cast<uint32_t>(i), nqu = static_cast<uint32_t>(nq);
+            r = iu / nqu;
+            qd = iu - static_cast<uint32_t>(r) * nqu;
+        } else {
+            r = i / nq;
+            qd = i - r * nq;
+        }
+        const int64_t b = r / M, row = r - b * M, col = qd * 4;
+        const float* src = partial + (b * splits) * slab + row * N + col;
+        float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+        if (vec && col + 4 <= N) {
+            int s = 0;
+            for (; s + 2 <= splits; s += 2) {  // two slabs in flight, added in order
+                const float4 p = __ldcg(reinterpret_cast<const float4*>(src + s * slab));
+                const float4 q = __ldcg(reinterpret_cast<const float4*>(src + (s + 1) * slab));
+                a0 += p.x;
+                a1 += p.y;
+                a2 += p.z;
+                a3 += p.w;
+                a0 += q.x;
+                a1 += q.y;
+                a2 += q.z;
+                a3 += q.w;
+            }
+            if (s < splits) {
+                const float4 p = __ldcg(reinterpret_cast<const float4*>(src + s * slab));
+                a0 += p.x;
+                a1 += p.y;
+                a2 += p.z;
+                a3 += p.w;
+            }
+        } else {
+            for (int s = 0; s < splits; ++s) {
+                const float* ps = src + s * slab;
+                a0 += __ldcg(ps);
+                if (col + 1 < N) a1 += __ldcg(ps + 1);
+                if (col + 2 < N) a2 += __ldcg(ps + 2);
+                if (col + 3 < N) a3 += __ldcg(ps + 3);
+            }
+        }
+        epi_store4(e, b, row, col, a0, a1, a2, a3);
+    }
 }
 
-__global__ void __launch_bounds__(256) skinny_reduce_kernel(const SkinnyParams sp) {
-    const int64_t total = sp.batch * sp.P * sp.Q;
-    const int64_t slab = sp.P * sp.Q;
-    if (sp.splits <= 16) {
-        for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-             i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-            const int64_t b = i / slab;
-            const float* src = sp.partial + b * sp.splits * slab + (i - b * slab);
-            float x[16];
-#pragma unroll
-            for (int s = 0; s < 16; ++s) x[s] = s < sp.splits ? __ldcg(src + s * slab) : 0.0f;
-            float y = 0.0f;
-#pragma unroll
-            for (int s = 0; s < 16; ++s)
-                if (s < sp.splits) y += x[s];
-            reduce_store(sp, i, y);
-        }
-        return;
-    }
-    __shared__ float part[8][33];
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    for (int64_t base = static_cast<int64_t>(blockIdx.x) * 32; base < total;
-         base += static_cast<int64_t>(gridDim.x) * 32) {
-        const int64_t i = base + lane;
-        float v = 0.0f;
-        if (i < total) {
-            const int64_t b = i / slab;
-            const float* src = sp.partial + b * sp.splits * slab + (i - b * slab);
-            int s = w;
-            for (; s + 24 < sp.splits; s += 32) {  // four loads in flight, summed in order
-                const float x0 = __ldcg(src + s * slab), x1 = __ldcg(src + (s + 8) * slab);
-                const float x2 = __ldcg(src + (s + 16) * slab), x3 = __ldcg(src + (s + 24) * slab);
-                v += x0;
-                v += x1;
-                v += x2;
-                v += x3;
-            }
-            for (; s < sp.splits; s += 8) v += __ldcg(src + s * slab);
-        }
-        part[w][lane] = v;
-        __syncthreads();
-        if (w == 0 && i < total) {
-            float y = 0.0f;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) y += part[k][lane];
-            reduce_store(sp, i, y);
-        }
-        __syncthreads();
-    }
-}
 
 }  // namespace
 
@@ -620,22 +614,59 @@ cudaError_t launch_tf32_split(const float* X, int64_t rows, int64_t cols, int64_
     return cudaGetLastError();
 }
 
+// The same reduction when there are many splits and few outputs: a block
+// takes 32 consecutive outputs and its 8 warps sum interleaved splits (warp w:
+// splits w, w+8, ...), combined through shared memory in warp order, so the
+// slab loads are spread over warps instead of one chain per output.
+__global__ void __launch_bounds__(256) split_reduce_wide_kernel(const float* __restrict__ partial,
+                                                                int64_t M, int64_t N,
+                                                                int64_t batch, int splits,
+                                                                EpiParams e) {
+    __shared__ float part[8][33];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t slab = M * N, total = batch * slab;
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * 32; base < total;
+         base += static_cast<int64_t>(gridDim.x) * 32) {
+        const int64_t i = base + lane;
+        float v = 0.0f;
+        int64_t b = 0, rc = 0;
+        if (i < total) {
+            b = i / slab;
+            rc = i - b * slab;
+            const float* src = partial + (b * splits) * slab + rc;
+            for (int s = w; s < splits; s += 8) v += __ldcg(src + s * slab);
+        }
+        part[w][lane] = v;
+        __syncthreads();
+        if (w == 0 && i < total) {
+            float y = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) y += part[k][lane];
+            const int64_t row = rc / N, col = rc - row * N;
+            epi_store1(e, b, row, col, y);
+        }
+        __syncthreads();
+    }
+}
+
 cudaError_t launch_split_reduce(const float* partial, int64_t M, int64_t N, int64_t batch,
                                 int splits, const EpiParams& e, const LaunchCtx& lc) {
-    SkinnyParams sp{};
-    sp.P = M;
-    sp.Q = N;
-    sp.batch = batch;
-    sp.splits = splits;
-    sp.p_is_m = 1;
-    sp.partial = const_cast<float*>(partial);
-    sp.e = e;
-    const int64_t outs = batch * M * N;
-    if (outs <= 0) return cudaSuccess;
+    const int64_t quads = batch * M * ((N + 3) / 4);
+    if (quads <= 0) return cudaSuccess;
     const int sms = lc.num_sms > 0 ? lc.num_sms : 148;
-    int64_t rb = splits <= 16 ? (outs + 255) / 256 : (outs + 31) / 32;
-    if (rb > static_cast<int64_t>(sms) * 8) rb = static_cast<int64_t>(sms) * 8;
-    skinny_reduce_kernel<<<static_cast<unsigned>(rb), 256, 0, lc.stream>>>(sp);
+    if (splits > 8 && quads < static_cast<int64_t>(sms) * 64) {
+        const int64_t outs = batch * M * N;
+        int64_t rb = (outs + 31) / 32;
+        if (rb > static_cast<int64_t>(sms) * 8) rb = static_cast<int64_t>(sms) * 8;
+        split_reduce_wide_kernel<<<static_cast<unsigned>(rb), 256, 0, lc.stream>>>(partial, M, N,
+                                                                                batch, splits, e);
+        return cudaGetLastError();
+    }
+    int64_t rb = (quads + 255) / 256;
+    if (rb > static_cast<int64_t>(sms) * 16) rb = static_cast<int64_t>(sms) * 16;
+    const int vec = (N % 4 == 0 && reinterpret_cast<uintptr_t>(partial) % 16 == 0) ? 1 : 0;
+    split_reduce_kernel<<<static_cast<unsigned>(rb), 256, 0, lc.stream>>>(partial, M, N, batch,
+                                                                          splits, vec, e);
     return cudaGetLastError();
 }
 
