@@ -63,18 +63,62 @@ __device__ __forceinline__ float ldf(const T* p) {
     return to_f<T>(__ldg(p));
 }
 
-// 16 raw bytes (VW elements of T): one 16-byte load when `vec` (aligned, all in
-// range), else up to n_valid element loads (zero-filled).  Kept raw so that
-// several loads can be in flight before any conversion.
+// VW elements at an unaligned (or short) position p: the 16-byte-aligned
+// chunk holding the first element and, only when the wanted bytes reach into
+// it, the next one; then a shift by the misalignment (the same for every lane
+// of a warp here, so the switch does not diverge).  Both chunks hold at least
+// one wanted element, so nothing outside the operand's pages is touched.
 template <typename T, int VW>
+__device__ __forceinline__ uint4 load_raw_unaligned(const T* p, int n_valid) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const uint4* base = reinterpret_cast<const uint4*>(a & ~static_cast<uintptr_t>(15));
+    const int sh = static_cast<int>(a & 15);  // bytes, a multiple of sizeof(T)
+    const uint4 lo = __ldg(base);
+    const uint4 hi = sh + n_valid * static_cast<int>(sizeof(T)) > 16 ? __ldg(base + 1)
+                                                                     : make_uint4(0, 0, 0, 0);
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    uint32_t o[4];
+    const int wo = sh >> 2;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t x0, x1;
+        switch (wo) {  // o[j] from words wo + j, wo + j + 1 (static indices only)
+            case 0: x0 = w[j]; x1 = w[j + 1]; break;
+            case 1: x0 = w[j + 1]; x1 = w[j + 2]; break;
+            case 2: x0 = w[j + 2]; x1 = w[j + 3]; break;
+            default: x0 = w[j + 3]; x1 = j + 4 < 8 ? w[j + 4] : 0u; break;
+        }
+        o[j] = (sh & 2) ? __funnelshift_r(x0, x1, 16) : x0;
+    }
+    uint4 r = make_uint4(o[0], o[1], o[2], o[3]);
+    if (n_valid < VW) {  // elements past n_valid read as zero
+        T* e = reinterpret_cast<T*>(&r);
+#pragma unroll
+        for (int i = 0; i < VW; ++i)
+            if (i >= n_valid) e[i] = T(0.0f);
+    }
+    return r;
+}
+
+// 16 raw bytes (VW elements of T): one 16-byte load when `vec` (aligned, all in
+// range); otherwise, with UA (the operand's rows are not 16-byte aligned), the
+// two-chunk shifted load above, and without it (only a short tail can miss
+// `vec`) up to n_valid element loads.  Zero-filled past n_valid.  Kept raw so
+// that several loads can be in flight before any conversion.
+template <typename T, int VW, bool UA>
 __device__ __forceinline__ uint4 load_raw(const T* p, bool vec, int n_valid) {
     if (vec) return __ldg(reinterpret_cast<const uint4*>(p));
-    uint4 r = make_uint4(0, 0, 0, 0);
-    T* e = reinterpret_cast<T*>(&r);
+    if constexpr (UA) {
+        if (n_valid <= 0) return make_uint4(0, 0, 0, 0);
+        return load_raw_unaligned<T, VW>(p, n_valid);
+    } else {
+        uint4 r = make_uint4(0, 0, 0, 0);
+        T* e = reinterpret_cast<T*>(&r);
 #pragma unroll
-    for (int i = 0; i < VW; ++i)
-        if (i < n_valid) e[i] = __ldg(p + i);
-    return r;
+        for (int i = 0; i < VW; ++i)
+            if (i < n_valid) e[i] = __ldg(p + i);
+        return r;
+    }
 }
 
 template <typename T, int VW>
@@ -153,8 +197,10 @@ __device__ __forceinline__ void skinny_out(const SkinnyParams& sp, int64_t b, in
 }
 
 // One warp per (batch, row q, split); lanes split the K range in 16-byte steps.
-// PMAX small-operand rows per pass (1, 4 or 16).
-template <typename T, int PMAX>
+// PMAX small-operand rows per pass (1, 4 or 16); UA: the streamed rows are not
+// 16-byte aligned (a separate instantiation, so the aligned one keeps its
+// registers).
+template <typename T, int PMAX, bool UA>
 __global__ void __launch_bounds__(256, PMAX == 1 ? 3 : 2) skinny_dot_kernel(const SkinnyParams sp) {
     constexpr int VW = 16 / sizeof(T);
     const int lane = threadIdx.x & 31;
@@ -172,7 +218,7 @@ __global__ void __launch_bounds__(256, PMAX == 1 ? 3 : 2) skinny_dot_kernel(cons
         const T* lrow = Lbase + b * sp.stride_l + q * sp.ldl;
         const T* sb = Sbase + b * sp.stride_s;
         // U 16-byte loads of the streamed row in flight per lane (fewer when P is large)
-        constexpr int U = PMAX == 1 ? 8 : PMAX == 4 ? 4 : 2;
+        constexpr int U = PMAX == 1 ? (UA ? 6 : 8) : PMAX == 4 ? 4 : 2;
         for (int64_t p0 = 0; p0 < sp.P; p0 += PMAX) {
             float acc[PMAX];
 #pragma unroll
@@ -183,7 +229,7 @@ __global__ void __launch_bounds__(256, PMAX == 1 ? 3 : 2) skinny_dot_kernel(cons
                 for (int u = 0; u < U; ++u) {
                     const int64_t k = kb + u * 32 * VW;
                     const int nv = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(VW), k1 - k)));
-                    raw[u] = load_raw<T, VW>(lrow + k, sp.l_vec && nv == VW, nv);
+                    raw[u] = load_raw<T, VW, UA>(lrow + k, sp.l_vec && nv == VW, nv);
                 }
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
@@ -274,7 +320,7 @@ __global__ void __launch_bounds__(256, PMAX == 1 ? 3 : PMAX == 4 ? 2 : 1)
             uint4 raw[G];
 #pragma unroll
             for (int u = 0; u < G; ++u)
-                if (u < gn) raw[u] = load_raw<T, VW>(lcol + (kb + u) * sp.ldl, vec, nv);
+                if (u < gn) raw[u] = load_raw<T, VW, true>(lcol + (kb + u) * sp.ldl, vec, nv);
 #pragma unroll
             for (int i = 0; i < PMAX; ++i) {
                 if (p0 + i >= sp.P) break;
@@ -476,7 +522,11 @@ cudaError_t launch_skinny(const gemm_config_t& cfg, const SkinnyArgs& a, const S
         int64_t blocks = (items + 7) / 8;
         if (blocks > static_cast<int64_t>(sms) * 16) blocks = static_cast<int64_t>(sms) * 16;
         const unsigned grid = static_cast<unsigned>(blocks > 0 ? blocks : 1);
-#define G13_DOT(T, PM) skinny_dot_kernel<T, PM><<<grid, 256, 0, lc.stream>>>(sp)
+#define G13_DOT(T, PM)                                                      \
+    do {                                                                    \
+        if (sp.l_vec) skinny_dot_kernel<T, PM, false><<<grid, 256, 0, lc.stream>>>(sp); \
+        else skinny_dot_kernel<T, PM, true><<<grid, 256, 0, lc.stream>>>(sp);           \
+    } while (0)
 #define G13_DOT_PM(T) \
     if (pm == 1) G13_DOT(T, 1); else if (pm == 4) G13_DOT(T, 4); else G13_DOT(T, 16)
         if (a.dtype == GEMM_F32) {
