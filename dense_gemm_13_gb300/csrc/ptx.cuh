@@ -103,6 +103,19 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// 4-byte asynchronous copy from global to shared memory; with `pred` false
+// nothing is read and the destination is zero-filled (src must still be a
+// valid address).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, bool pred) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(pred ? 4 : 0)
+                 : "memory");
+}
+// Waits for all of this thread's cp.async copies.
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // 3-D tiled store of one box from shared memory (bulk-group completion).
 // Out-of-range parts of the box are not written.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, uint32_t src, int32_t c0,

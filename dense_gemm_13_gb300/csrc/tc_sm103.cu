@@ -726,34 +726,107 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                     break;
                 }
             } else {
+                // C rows TMA cannot address (row stride, batch stride or base not a
+                // multiple of 16 bytes, e.g. N odd).  Each thread holds one row of a
+                // 32-row x 32-column chunk; the warp turns the chunk around in its
+                // staging buffer so that every store (and every residual load)
+                // covers 32 consecutive columns of one row instead of one column of
+                // 32 rows.  The buffer has the layout of the TMA path: 16-byte piece
+                // j of row r at r * 128 + ((j ^ (r & 7)) << 4), so row-wise
+                // (16-byte) and column-wise (4-byte) accesses are both free of bank
+                // conflicts.
+                uint8_t* sb = etile;
+                uint8_t* rowp = sb + lane * 128;
+                const uint32_t colx = ((lane >> 2) << 4) | ((lane & 3) << 2);  // column `lane`
+                const int rows_here =
+                    static_cast<int>(max(int64_t(0), min(int64_t(32), e.M - row0)));
+                const bool smx = e.act == GEMM_ACT_SOFTMAX;  // v holds exp(t - max)
 #pragma unroll 1
-                for (int c = c_lo / 32; c < (c_lo + SLICE) / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c * 32), r);
+                for (int c = c_lo; c < c_lo + SLICE; c += 32) {
+                    const int64_t cg = col0 + c;
+                    const int ncol = static_cast<int>(max(int64_t(0), min(int64_t(32), e.N - cg)));
+                    const bool with_r = ncol > 0 && !smx && !args.epi_plain && e.R;
+                    __syncwarp();  // the previous chunk's reads of the buffer are done
+                    if (with_r) {
+                        // The residual goes out first, as asynchronous copies straight into
+                        // the buffer (lane = column: 32 coalesced row segments), so that
+                        // it overlaps the accumulator load and holds no registers.
+                        const float* rp =
+                            e.R + bt * e.stride_r + static_cast<int64_t>(row0) * e.ldr + cg + lane;
+#pragma unroll
+                        for (int r = 0; r < 32; ++r) {
+                            const bool in = r < rows_here && lane < ncol;
+                            cp_async_4(smem_u32(sb + r * 128 + (colx ^ ((r & 7) << 4))),
+                                       in ? rp + r * e.ldr : e.R, in);
+                        }
+                    }
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c), v);
                     tmem_ld_wait();
-                    if (c == (c_lo + SLICE) / 32 - 1) {
+                    if (c + 32 >= c_lo + SLICE) {
                         // All of this buffer is in registers: hand it back to the MMA warp.
                         release(buf);
                     }
-                    if (col0 + c * 32 < e.N && e.act == GEMM_ACT_SOFTMAX) {
-                        // the probabilities, then a plain store (cast only)
-                        EpiParams ep = e;
-                        ep.alpha = 1.0f;
-                        ep.bias = nullptr;
-                        ep.act = GEMM_ACT_NONE;
-                        float pr[32];
+                    if (ncol == 0) continue;
+                    if (with_r) {
+                        cp_async_wait_all();
+                        __syncwarp();
+                    }
+                    float y[32];
+                    const float sc = smx ? sinv : e.alpha;
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) pr[i] = __uint_as_float(r[i]) * sinv;
+                    for (int i = 0; i < 32; ++i) y[i] = __uint_as_float(v[i]) * sc;
+                    if (!smx && !args.epi_plain) {
+                        if (e.bias) {
 #pragma unroll
-                        for (int g = 0; g < 8; ++g)
-                            epi_store4(ep, b, row, col0 + c * 32 + 4 * g, pr[4 * g], pr[4 * g + 1],
-                                       pr[4 * g + 2], pr[4 * g + 3]);
-                    } else if (col0 + c * 32 < e.N) {
+                            for (int i = 0; i < 32; ++i)
+                                if (i < ncol) y[i] += __ldg(e.bias + cg + i);
+                        }
+                        if (e.act == GEMM_ACT_GELU_ERF) {
 #pragma unroll
-                        for (int g = 0; g < 8; ++g)
-                            epi_store4(e, b, row, col0 + c * 32 + 4 * g, __uint_as_float(r[4 * g]),
-                                       __uint_as_float(r[4 * g + 1]), __uint_as_float(r[4 * g + 2]),
-                                       __uint_as_float(r[4 * g + 3]));
+                            for (int i = 0; i < 32; ++i) y[i] = gelu_as7126(y[i]);
+                        } else if (e.act == GEMM_ACT_RELU) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) y[i] = fmaxf(y[i], 0.0f);
+                        }
+                        if (with_r) {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const float4 r4 =
+                                    *reinterpret_cast<const float4*>(rowp + ((j ^ (lane & 7)) << 4));
+                                y[4 * j] += e.beta * r4.x;
+                                y[4 * j + 1] += e.beta * r4.y;
+                                y[4 * j + 2] += e.beta * r4.z;
+                                y[4 * j + 3] += e.beta * r4.w;
+                            }
+                        }
+                    }
+                    // this thread's row into the buffer, then the buffer out by rows
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<float4*>(rowp + ((j ^ (lane & 7)) << 4)) =
+                            make_float4(y[4 * j], y[4 * j + 1], y[4 * j + 2], y[4 * j + 3]);
+                    __syncwarp();
+                    if (lane < ncol) {
+                        const int64_t off =
+                            b * e.stride_c + static_cast<int64_t>(row0) * e.ldc + cg + lane;
+                        const auto at = [&](int r) {
+                            return *reinterpret_cast<const float*>(sb + r * 128 +
+                                                                   (colx ^ ((r & 7) << 4)));
+                        };
+                        if (e.out_dtype == GEMM_F32) {
+                            float* cp = static_cast<float*>(e.C) + off;
+#pragma unroll 8
+                            for (int r = 0; r < rows_here; ++r) cp[r * e.ldc] = at(r);
+                        } else if (e.out_dtype == GEMM_BF16) {
+                            __nv_bfloat16* cp = static_cast<__nv_bfloat16*>(e.C) + off;
+#pragma unroll 8
+                            for (int r = 0; r < rows_here; ++r) cp[r * e.ldc] = __float2bfloat16_rn(at(r));
+                        } else {
+                            __half* cp = static_cast<__half*>(e.C) + off;
+#pragma unroll 8
+                            for (int r = 0; r < rows_here; ++r) cp[r * e.ldc] = __float2half_rn(at(r));
+                        }
                     }
                 }
             }
