@@ -331,14 +331,15 @@ int check_config(const Problem& p, const gemm_config_t& in, gemm_config_t* out) 
                   (c.variant == 1 && ((c.bn == 256 && c.stages == 3) ||
                                       (c.bn == 128 && c.stages == 4) ||
                                       (c.bn == 512 && c.stages == 1))) ||
-                  (c.variant == 2 && c.bn == 256 && (c.stages == 6 || c.stages == 4))))
+                  (c.variant == TC_VARIANT_PAIR && c.bn == 256 && (c.stages == 6 || c.stages == 4))))
                 return GEMM_ERR_UNSUPPORTED;
-            if (c.variant == 2 && c.split_k > 1) return GEMM_ERR_UNSUPPORTED;
+
+            if (tc_is_pair(c) && c.split_k > 1) return GEMM_ERR_UNSUPPORTED;
             // 512-wide tiles exist for the row softmax; the softmax needs the whole
             // row in one tile with one epilogue thread per row
             if (c.bn == 512 && p.epi.act != GEMM_ACT_SOFTMAX) return GEMM_ERR_UNSUPPORTED;
             if (p.epi.act == GEMM_ACT_SOFTMAX &&
-                (c.variant == TC_VARIANT_PAIR || c.split_k > 1 || c.bn < p.N))
+                (tc_is_pair(c) || c.split_k > 1 || c.bn < p.N))
                 return GEMM_ERR_UNSUPPORTED;
             if (c.raster_group == 0) c.raster_group = 16;
             break;

@@ -101,6 +101,7 @@ struct TcArgs {
     int a_bmul, b_bmul;
     int epi_tma;    // 1: C is written by TMA stores through shared memory
     int r_tma;      // 1: the FP32 residual is read by TMA loads (implies epi_tma)
+    int r_ahead;    // 1: each chunk's residual is requested one chunk ahead (implies r_tma)
     int out16;      // 1: C holds 16-bit values (64 columns per 128-byte chunk)
     int c_bmul, r_bmul;
     int c_smul;     // split-K: C batch coordinate = b * c_bmul + split * c_smul
@@ -178,7 +179,7 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
     // Accumulator buffers in TMEM: two of BN columns, or one for 512-wide
     // tiles (the row softmax), which fill all 512 columns.
     constexpr int NBUF = BN > 256 ? 1 : 2;
-    constexpr uint32_t TMEM_COLS = NBUF * BN;  // 256 or 512: powers of two
+    constexpr uint32_t TMEM_COLS = NBUF * BN <= 256 ? 256u : 512u;  // allocations: powers of two
     constexpr int NHALF = BN > 256 ? 2 : 1;    // MMAs per K step (N <= 256 per MMA)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -449,6 +450,37 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
         const EpiParams& e = args.e;
         uint32_t rph = 0;  // bit i: phase parity of rb[i]
         int nchunk = 0;    // chunks this warp has staged (selects the buffer)
+        // Residual by TMA, when the host asks for it (args.r_ahead: short K or one
+        // tile per CTA, where the epilogue is not hidden behind a next main loop):
+        // the tile of chunk k + 1 is requested while chunk k is being worked on,
+        // so its load overlaps a whole chunk (the first one overlaps the first
+        // main loop).  r_ahead = index of the chunk whose residual is already in
+        // flight (-1: none).
+        int r_ahead = -1;
+        // TMA coordinates are 32-bit: (column, row, batch coordinate).
+        const auto r_issue = [&](int sel, int32_t cg, int32_t r0, int32_t bc) {
+            mbar_arrive_expect_tx(smem_u32(&rb[sel]), EPI_BUF_BYTES);
+            tma_load_3d(smem_u32(etile + sel * EPI_BUF_BYTES), &tmR, smem_u32(&rb[sel]), cg, r0,
+                        bc);
+        };
+        // First chunk of work item t for this warp: its column, row and residual
+        // batch coordinate; false when the item has no columns for this warp.
+        // (The residual is never read under split-K, so work items are tiles.)
+        const auto first_chunk = [&](int64_t t, int32_t& cg, int32_t& r0, int32_t& bc) {
+            int64_t bidx, mt2, nt2;
+            tc_tile_coords(t, args, bidx, mt2, nt2);
+            cg = static_cast<int32_t>(nt2) * BN + c_lo;
+            r0 = static_cast<int32_t>(mt2) * L::TILE_M + static_cast<int32_t>(rank * TBM + q * 32);
+            bc = static_cast<int32_t>(bidx) * args.r_bmul;
+            return cg < e.N;
+        };
+        if (args.r_ahead && first_item < args.total_items) {
+            int32_t cg, r0, bidx;
+            if (first_chunk(first_item, cg, r0, bidx)) {
+                if (lane == 0) r_issue(0, cg, r0, bidx);
+                r_ahead = 0;
+            }
+        }
         bool ok = true;
         int lt = 0;
         for (int64_t t = first_item; ok && t < args.total_items; t += item_stride, ++lt) {
@@ -580,19 +612,37 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                     }
                     const int64_t cg = col0 + c;  // first global column of the chunk
                     if (cg >= e.N) continue;
-                    const int sel = nchunk & 1;
+                    const int k = nchunk;
+                    const int sel = k & 1;
                     ++nchunk;
                     uint8_t* sb = etile + sel * EPI_BUF_BYTES;
-                    // The TMA store issued from this buffer two chunks ago must
-                    // have finished reading it.
-                    if (lane == 0) bulk_wait_read<1>();
-                    __syncwarp();
-                    if (args.r_tma && lane == 0) {
-                        mbar_arrive_expect_tx(smem_u32(&rb[sel]), EPI_BUF_BYTES);
-                        tma_load_3d(smem_u32(sb), &tmR, smem_u32(&rb[sel]),
-                                    static_cast<int32_t>(cg), row0,
-                                    static_cast<int32_t>(bt * args.r_bmul));
+                    if (!args.r_tma) {
+                        // The TMA store issued from this buffer two chunks ago must
+                        // have finished reading it.
+                        if (lane == 0) bulk_wait_read<1>();
+                    } else {
+                        if (r_ahead != k && lane == 0) {
+                            bulk_wait_read<1>();
+                            r_issue(sel, static_cast<int32_t>(cg), row0,
+                                    static_cast<int32_t>(bt) * args.r_bmul);
+                        }
+                        // Next chunk: the rest of this tile, else the first chunk of
+                        // this warp's next work item.
+                        int32_t cn = static_cast<int32_t>(cg) + W, rn = row0,
+                                bn = static_cast<int32_t>(bt) * args.r_bmul;
+                        bool has_next = args.r_ahead && c + W < c_lo + SLICE && cn < e.N;
+                        if (args.r_ahead && !has_next && t + item_stride < args.total_items)
+                            has_next = first_chunk(t + item_stride, cn, rn, bn);
+                        if (has_next) {
+                            // its buffer was read by the store of the previous chunk
+                            if (lane == 0) {
+                                bulk_wait_read<0>();
+                                r_issue(sel ^ 1, cn, rn, bn);
+                            }
+                            r_ahead = k + 1;
+                        }
                     }
+                    __syncwarp();
                     float y[W];
                     const bool smx = e.act == GEMM_ACT_SOFTMAX;  // v holds exp(t - max)
                     // 16-byte chunk j of this thread's row sits at position j ^ (row & 7).
@@ -831,6 +881,10 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                 }
             }
         }
+        // A residual load for a chunk that was never reached (the loop gave up)
+        // must land before the CTA's shared memory goes away.
+        if (r_ahead >= nchunk && lane == 0)
+            tc_drain(smem_u32(&rb[r_ahead & 1]), (rph >> (r_ahead & 1)) & 1u, tmo);
         // Shared memory must outlive the TMA stores that read it.
         if (lane == 0) bulk_wait_all();
         __syncwarp();
@@ -865,6 +919,7 @@ cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& 
     static const CUtensorMap unused_map{};
     a.epi_tma = em != nullptr;
     a.r_tma = em != nullptr && em->r_tma;
+    a.r_ahead = 0;  // set below, once the grid is known
     a.out16 = e.out_dtype != GEMM_F32;
     a.c_bmul = em ? em->c_bmul : 0;
     a.c_smul = em ? em->c_smul : 0;
@@ -932,12 +987,14 @@ cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& 
         if (pairs > a.total_items) pairs = a.total_items;
         if (pairs < 1) pairs = 1;
         lcfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+        a.r_ahead = a.r_tma && (a.k_blocks <= 8 || a.total_items <= pairs);
         err2 = cudaLaunchKernelEx(&lcfg, kern, tmA, tmB, mc, mr, a);
         return err2;
     }
     int64_t grid = cfg.num_ctas > 0 ? cfg.num_ctas : lc.num_sms;
     if (grid > a.total_items) grid = a.total_items;
     if (grid < 1) grid = 1;
+    a.r_ahead = a.r_tma && (a.k_blocks <= 8 || a.total_items <= grid);
     kern<<<static_cast<unsigned>(grid), tc_threads<EW>(), smem, lc.stream>>>(tmA, tmB, mc, mr, a);
     err2 = cudaGetLastError();
     if (err2 != cudaSuccess || a.splits == 1) return err2;

@@ -96,6 +96,23 @@ def test_tc_pair_epilogue_batched():
         full_check(Run(w, config=g13.Config("tc", 128, 256, 64, 4, variant=2), ldc_pad=1))
 
 
+RES_CONFIGS = [g13.Config("tc", 128, 256, 64, 3, variant=1, num_ctas=3),
+               g13.Config("tc", 128, 128, 64, 6, num_ctas=5),
+               g13.Config("tc", 128, 256, 64, 6, variant=2, num_ctas=2)]
+
+
+@pytest.mark.parametrize("K", [300, 700])
+@pytest.mark.parametrize("cfg", RES_CONFIGS, ids=lambda c: f"bn{c.bn}v{c.variant}x{c.num_ctas}")
+def test_tc_residual_across_tiles(cfg, K):
+    # FP32 residual read by TMA with many tiles per CTA (or pair), ragged M and N:
+    # with 5 K blocks the kernel requests each chunk's residual one chunk ahead,
+    # also across tile boundaries; with 11 K blocks and several tiles per CTA it
+    # reads each chunk's residual when it gets there.
+    w = Workload(f"tc_res_{K}", "bf16", 520, 700, K, batch=2, b_layout="nk", bias=True,
+                 act="relu", residual=True, alpha=0.5, beta=0.75)
+    full_check(Run(w, config=cfg))
+
+
 # ---------------------------------------------------------------- 3xTF32 (FP32 on tensor cores)
 TF32X3_CONFIGS = [g13.Config("tf32x3", 128, 256, 32, 3, variant=2),
                   g13.Config("tf32x3", 128, 128, 32, 3)]
