@@ -30,16 +30,68 @@
 namespace g13 {
 namespace {
 
-template <typename T>
-__global__ void stage_copy_kernel(const T* __restrict__ src, int64_t rows, int64_t cols, int64_t ld,
-                                  int64_t bstride, int64_t batch, T* __restrict__ dst,
-                                  int64_t dst_ld) {
-    const int64_t total_rows = rows * batch;
-    for (int64_t r = blockIdx.x; r < total_rows; r += gridDim.x) {
+// Bytes [sh, sh + 16) of the 32-byte window lo:hi (sh even).  The shift is
+// the same for every lane of a warp here, so the switch does not diverge.
+__device__ __forceinline__ uint4 window16(const uint4& lo, const uint4& hi, int sh) {
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    const uint32_t sel = 0x3210u + static_cast<uint32_t>(sh & 3) * 0x1111u;
+    switch (sh >> 2) {
+        case 0:
+            return make_uint4(__byte_perm(w[0], w[1], sel), __byte_perm(w[1], w[2], sel),
+                              __byte_perm(w[2], w[3], sel), __byte_perm(w[3], w[4], sel));
+        case 1:
+            return make_uint4(__byte_perm(w[1], w[2], sel), __byte_perm(w[2], w[3], sel),
+                              __byte_perm(w[3], w[4], sel), __byte_perm(w[4], w[5], sel));
+        case 2:
+            return make_uint4(__byte_perm(w[2], w[3], sel), __byte_perm(w[3], w[4], sel),
+                              __byte_perm(w[4], w[5], sel), __byte_perm(w[5], w[6], sel));
+        default:
+            return make_uint4(__byte_perm(w[3], w[4], sel), __byte_perm(w[4], w[5], sel),
+                              __byte_perm(w[5], w[6], sel), __byte_perm(w[6], w[7], sel));
+    }
+}
+
+// Work unit = (row, 128 consecutive 16-byte pieces of the padded destination
+// row); a warp's lane takes pieces lane, lane + 32, lane + 64, lane + 96 and
+// issues all their loads before the stores, so a warp keeps up to 8 KB of
+// reads in flight.  Piece j comes from the one or two aligned 16-byte source
+// pieces that hold its bytes, shifted by the row's misalignment.  A source
+// piece is read only when it holds a wanted byte, so nothing outside the
+// operand's pages is touched.  Destination bytes past the row's end (padding
+// up to dst_ld) get whatever the last source piece holds there; the GEMM's
+// tensor maps end at the row's last column and never read them.
+constexpr int STAGE_PIECES = 4;  // per lane per unit
+__global__ void stage_copy_kernel(const uint8_t* __restrict__ src, int64_t rows, int64_t row_bytes,
+                                  int64_t ld_bytes, int64_t bstride_bytes, int64_t batch,
+                                  uint8_t* __restrict__ dst, int64_t dst_ld_bytes) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    const int64_t npiece = (row_bytes + 15) / 16;
+    const int64_t per_row = (npiece + 32 * STAGE_PIECES - 1) / (32 * STAGE_PIECES);
+    const int64_t units = rows * batch * per_row;
+    for (int64_t u = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+         u < units; u += warps) {
+        const int64_t r = u / per_row;
+        const int64_t j0 = (u - r * per_row) * (32 * STAGE_PIECES) + lane;
         const int64_t b = r / rows, i = r - b * rows;
-        const T* s = src + b * bstride + i * ld;
-        T* d = dst + r * dst_ld;
-        for (int64_t c = threadIdx.x; c < cols; c += blockDim.x) d[c] = s[c];
+        const uintptr_t a = reinterpret_cast<uintptr_t>(src + b * bstride_bytes + i * ld_bytes);
+        const int sh = static_cast<int>(a & 15);
+        const uint4* base = reinterpret_cast<const uint4*>(a - sh);
+        uint4* d = reinterpret_cast<uint4*>(dst + r * dst_ld_bytes);
+        uint4 lo[STAGE_PIECES], hi[STAGE_PIECES];
+#pragma unroll
+        for (int q = 0; q < STAGE_PIECES; ++q) {
+            const int64_t j = j0 + 32 * q;
+            const int64_t left = row_bytes - 16 * j;  // wanted bytes from piece j on
+            lo[q] = j < npiece ? __ldg(base + j) : make_uint4(0, 0, 0, 0);
+            hi[q] = j < npiece && sh + (left < 16 ? left : 16) > 16 ? __ldg(base + j + 1)
+                                                                   : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int q = 0; q < STAGE_PIECES; ++q) {
+            const int64_t j = j0 + 32 * q;
+            if (j < npiece) d[j] = window16(lo[q], hi[q], sh);
+        }
     }
 }
 
@@ -446,16 +498,16 @@ cudaError_t launch_stage_copy(const void* src, int64_t rows, int64_t cols, int64
                               cudaStream_t stream) {
     const int64_t total = rows * batch;
     if (total <= 0 || cols <= 0) return cudaSuccess;
-    const unsigned grid = static_cast<unsigned>(total < 65536 ? total : 65536);
-    const int threads = cols >= 256 ? 256 : 128;
-    if (esz == 2)
-        stage_copy_kernel<uint16_t><<<grid, threads, 0, stream>>>(
-            static_cast<const uint16_t*>(src), rows, cols, ld, bstride, batch,
-            static_cast<uint16_t*>(dst), dst_ld);
-    else
-        stage_copy_kernel<float><<<grid, threads, 0, stream>>>(static_cast<const float*>(src), rows,
-                                                               cols, ld, bstride, batch,
-                                                               static_cast<float*>(dst), dst_ld);
+    if (reinterpret_cast<uintptr_t>(dst) % 16 != 0 || (dst_ld * esz) % 16 != 0)
+        return cudaErrorInvalidValue;
+    // 8 warps per block, at most 8 blocks per SM's worth of work units
+    const int64_t npiece = (cols * esz + 15) / 16;
+    const int64_t units = total * ((npiece + 127) / 128);
+    const int64_t blocks = (units + 7) / 8;
+    const unsigned grid = static_cast<unsigned>(blocks < 152 * 8 ? blocks : 152 * 8);
+    stage_copy_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint8_t*>(src), rows, cols * esz,
+                                                ld * esz, bstride * esz, batch,
+                                                static_cast<uint8_t*>(dst), dst_ld * esz);
     return cudaGetLastError();
 }
 

@@ -120,8 +120,9 @@ cudaError_t launch_skinny(const gemm_config_t& cfg, const SkinnyArgs& a, const S
 void skinny_geometry(int64_t M, int64_t N, int b_layout, int64_t* P, int64_t* Q, int* dot);
 
 // Copies [batch][rows][cols] (row stride ld, batch stride bstride, element
-// size esz) into a dense [batch][rows][dst_ld] buffer.  Padding columns are
-// left untouched.
+// size esz) into a dense [batch][rows][dst_ld] buffer (dst and dst_ld * esz
+// multiples of 16 bytes, else cudaErrorInvalidValue).  Padding columns get
+// unspecified bytes: the tensor maps over the copy end at column cols.
 cudaError_t launch_stage_copy(const void* src, int64_t rows, int64_t cols, int64_t ld,
                               int64_t bstride, int64_t batch, int esz, void* dst,
                               int64_t dst_ld, cudaStream_t stream);
