@@ -298,7 +298,10 @@ def sweep_summary(g13, torch, device, pk, pk_kind, reps=8):
     Buckets by the dispatcher's kernel and regime: skinny (M or N <= 4), tensor-core
     problems that are HBM-bound by their arithmetic intensity, and compute-bound ones.
     Each triple: 2 warm-up runs, then `reps` runs each between an L2 flush and a CUDA
-    event pair; median time.  Roofline fraction as in the main line.
+    event pair; median time.  Roofline fraction as in the main line.  Besides the
+    medians (which the many launch-latency-bound tiny triples dominate), each bucket
+    and the whole sweep report aggregate_frac = sum of the triples' roofline times /
+    sum of their measured times: the fraction for running the bucket as one job.
     """
     from dense_gemm_13_gb300.inputs import SWEEP_SIZES, sweep_workload
     big = max(SWEEP_SIZES)
@@ -350,8 +353,13 @@ def sweep_summary(g13, torch, device, pk, pk_kind, reps=8):
                        "median_tflops": round(statistics.median(x[1] for x in sel), 3),
                        "median_frac": round(statistics.median(x[2] for x in sel), 4),
                        "min_frac": round(min(x[2] for x in sel), 4),
-                       "max_frac": round(max(x[2] for x in sel), 4)}
+                       "max_frac": round(max(x[2] for x in sel), 4),
+                       # the bucket as one job: sum of roofline times / sum of measured times
+                       "aggregate_frac": round(sum(x[2] * x[3] for x in sel) /
+                                               sum(x[3] for x in sel), 4),
+                       "ms": round(sum(x[3] for x in sel), 3)}
     out["total_ms"] = round(sum(x[3] for x in rows), 3)
+    out["aggregate_frac"] = round(sum(x[2] * x[3] for x in rows) / sum(x[3] for x in rows), 4)
     return out
 
 
