@@ -55,27 +55,61 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
-// GELU for the tensor-core epilogue, 0.5 y (1 + erf(y / sqrt 2)), with erf
-// from Abramowitz & Stegun, Handbook of Mathematical Functions, formula
-// 7.1.26 (|error| <= 1.5e-7 on erf): for x >= 0,
-//     erf(x) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-x^2),
+// Two FP32 values in one 64-bit register pair, for Blackwell's packed FP32
+// arithmetic (mul / fma .rn.f32x2: two IEEE operations per instruction).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// GELU for the tensor-core epilogue, 0.5 y (1 + erf(y / sqrt 2)), two values
+// at a time, with erf from Abramowitz & Stegun, Handbook of Mathematical
+// Functions, formula 7.1.26 (|error| <= 1.5e-7 on erf): for x >= 0,
+//     1 - erf(x) = (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-x^2),
 //     t = 1 / (1 + p x),  p = 0.3275911,
-//     a1..a5 = 0.254829592, -0.284496736, 1.421413741, -1.453152027, 1.061405429,
-// and erf(-x) = -erf(x).  Two MUFU operations (reciprocal, exp2) and five
-// FMAs: the library erff made GELU 44 % of an FFN-shaped GEMM's time.
-__device__ __forceinline__ float gelu_as7126(float y) {
-    const float x = fabsf(y) * 0.70710678118654752f;
-    float t;  // 1 / (1 + p x) by the MUFU approximation (~1 ulp)
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(fmaf(0.3275911f, x, 1.0f)));
-    float p = fmaf(1.061405429f, t, -1.453152027f);
-    p = fmaf(p, t, 1.421413741f);
-    p = fmaf(p, t, -0.284496736f);
-    p = fmaf(p, t, 0.254829592f);
-    p *= t;
-    const float e = ex2_approx(-x * x * 1.4426950408889634f);  // exp(-x^2)
-    const float erf_abs = fmaf(-p, e, 1.0f);
-    const float erf_v = y < 0.0f ? -erf_abs : erf_abs;
-    return 0.5f * y * (1.0f + erf_v);
+//     a1..a5 = 0.254829592, -0.284496736, 1.421413741, -1.453152027, 1.061405429.
+// With h = 1 - erf(|y| / sqrt 2), GELU(y) = max(y, 0) - 0.5 |y| h for either
+// sign of y (erf is odd).  Per pair of values: two MUFU reciprocals, two MUFU
+// exp2, and nine packed FP32 operations (the library erff made GELU 44 % of an
+// FFN-shaped GEMM's time; scalar arithmetic took twice the instructions).
+__device__ __forceinline__ void gelu2_as7126(float& y0, float& y1) {
+    const uint64_t ax = f2_pack(fabsf(y0), fabsf(y1));
+    // 1 + p |y| / sqrt 2, p = 0.3275911
+    const uint64_t u = f2_fma(ax, f2_pack(0.23164189f, 0.23164189f), f2_pack(1.0f, 1.0f));
+    float u0, u1;
+    f2_unpack(u, u0, u1);
+    float t0, t1;  // 1 / u by the MUFU approximation (~1 ulp)
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t0) : "f"(u0));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t1) : "f"(u1));
+    const uint64_t t = f2_pack(t0, t1);
+    uint64_t p = f2_fma(f2_pack(1.061405429f, 1.061405429f), t, f2_pack(-1.453152027f, -1.453152027f));
+    p = f2_fma(p, t, f2_pack(1.421413741f, 1.421413741f));
+    p = f2_fma(p, t, f2_pack(-0.284496736f, -0.284496736f));
+    p = f2_fma(p, t, f2_pack(0.254829592f, 0.254829592f));
+    p = f2_mul(p, t);
+    const uint64_t y = f2_pack(y0, y1);
+    // exponent of exp(-y^2 / 2) in base 2: -y^2 log2(e) / 2
+    const uint64_t q = f2_mul(f2_mul(y, f2_pack(-0.72134752044448170f, -0.72134752044448170f)), y);
+    float q0, q1;
+    f2_unpack(q, q0, q1);
+    const uint64_t h = f2_mul(p, f2_pack(ex2_approx(q0), ex2_approx(q1)));
+    const uint64_t r = f2_fma(f2_mul(ax, h), f2_pack(-0.5f, -0.5f),
+                              f2_pack(fmaxf(y0, 0.0f), fmaxf(y1, 0.0f)));
+    f2_unpack(r, y0, y1);
 }
 
 constexpr int TBM = 128, TBK = 64;        // rows of A per CTA; K elements per stage (16-bit)
@@ -678,8 +712,7 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                         }
                         if (e.act == GEMM_ACT_GELU_ERF) {
 #pragma unroll
-                            for (int i = 0; i < W; ++i)
-                                if (i < W) y[i] = gelu_as7126(y[i]);
+                            for (int i = 0; i < W; i += 2) gelu2_as7126(y[i], y[i + 1]);
                         } else if (e.act == GEMM_ACT_RELU) {
 #pragma unroll
                             for (int i = 0; i < W; ++i)
@@ -834,7 +867,7 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                         }
                         if (e.act == GEMM_ACT_GELU_ERF) {
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) y[i] = gelu_as7126(y[i]);
+                            for (int i = 0; i < 32; i += 2) gelu2_as7126(y[i], y[i + 1]);
                         } else if (e.act == GEMM_ACT_RELU) {
 #pragma unroll
                             for (int i = 0; i < 32; ++i) y[i] = fmaxf(y[i], 0.0f);
