@@ -394,6 +394,12 @@ int gemm_run(gemm_plan_t plan, const void* A, const void* B, void* C, const void
         ce = launch_skinny(cfg, a, s, e, lc);
         return map_cuda_error(ce);
     }
+    if (ffma_small(cfg)) {
+        ce = launch_ffma_small(static_cast<const float*>(A), static_cast<const float*>(B), p.lda,
+                               p.ldb, ep.batch > 1 ? ep.stride_a : 0, ep.batch > 1 ? ep.stride_b : 0,
+                               ep.b_layout, s, e, st);
+        return map_cuda_error(ce);
+    }
 
     const OperandGeom ga = geom_a(p), gb = geom_b(p);
     CUtensorMap mA, mB;

@@ -236,6 +236,21 @@ int choose_config(const Problem& p, int num_sms, gemm_config_t* out) {
         const int64_t tiles = bt * cdiv(M, 128) * cdiv(N, c.bn);
         const int64_t waves = cdiv(tiles, slots);
         c.stream_k = (tiles * 10 < waves * slots * 9) ? 1 : 0;
+        // A few 128 x 128 tiles (at most one per eight SMs, e.g. 256^3 or 512^2)
+        // and K <= 512: split over stream-K, each tile's fix-up chain of partial
+        // sums costs more than the FMAs; 32 x 32 tiles from plain loads spread the
+        // work instead (GB300: 256^3 13.0 vs 25.3 us, 512^3 31.5 vs 47.6 us; with
+        // longer K stream-K's split of K wins: 512 x 512 x 1024 49.9 vs 58.0 us).
+        if (!wide && K <= 512 && bt * cdiv(M, 128) * cdiv(N, 128) * 8 <= num_sms &&
+            cdiv(M, 32) <= 65535 && bt <= 65535) {
+            c.variant = FFMA_VARIANT_SMALL;
+            c.bm = c.bn = c.bk = 32;
+            c.stages = 2;
+            c.raster_group = 1;
+            c.stream_k = 0;
+            *out = c;
+            return GEMM_OK;
+        }
     } else {
         c.kernel = GEMM_KERNEL_TC;
         c.bm = 128;
@@ -301,6 +316,16 @@ int check_config(const Problem& p, const gemm_config_t& in, gemm_config_t* out) 
             break;
         case GEMM_KERNEL_FFMA:
             if (p.dtype != GEMM_F32 || p.K == 0) return GEMM_ERR_UNSUPPORTED;
+            if (c.variant == FFMA_VARIANT_SMALL) {
+                // 32 x 32 tiles from plain loads: no stream-K, no staging
+                if (c.bm != 32 || c.bn != 32 || c.bk != 32 || c.stream_k != 0)
+                    return GEMM_ERR_UNSUPPORTED;
+                c.stages = 2;
+                c.stage_a = c.stage_b = 0;
+                if (c.raster_group == 0) c.raster_group = 1;
+                *out = c;
+                return GEMM_OK;
+            }
             if (c.variant < 0 || c.variant > 1) return GEMM_ERR_UNSUPPORTED;
             if (c.stream_k < 0 || c.stream_k > 1) return GEMM_ERR_UNSUPPORTED;
             if (c.bm != 128 || c.bk != 32) return GEMM_ERR_UNSUPPORTED;

@@ -91,6 +91,17 @@ inline int tc_b_box_rows(const gemm_config_t& cfg) {
     return rows < 256 ? rows : 256;
 }
 
+// FP32 FFMA config variant for problems with too few 128-row tiles to fill the
+// GPU: 32 x 32 tiles from plain loads (any stride or alignment, no TMA, no
+// staging, no workspace).
+constexpr int FFMA_VARIANT_SMALL = 2;
+inline bool ffma_small(const gemm_config_t& c) {
+    return c.kernel == GEMM_KERNEL_FFMA && c.variant == FFMA_VARIANT_SMALL;
+}
+cudaError_t launch_ffma_small(const float* A, const float* B, int64_t lda, int64_t ldb,
+                              int64_t stride_a, int64_t stride_b, int b_layout, const Shape& s,
+                              const EpiParams& e, cudaStream_t stream);
+
 // FP32 FFMA path: A via tmA (dims K, M, batch), B via tmB (KN: N, K, batch; NK: K, N, batch).
 cudaError_t launch_ffma(const gemm_config_t& cfg, int b_layout, const CUtensorMap& tmA,
                         const CUtensorMap& tmB, const Shape& s, const EpiParams& e,

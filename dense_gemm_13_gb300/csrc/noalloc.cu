@@ -152,7 +152,7 @@ extern "C" int gemm_run_noalloc(gemm_dtype_t dtype, int64_t M, int64_t N, int64_
     cfg.split_k = 1;   // the skinny kernel runs K unsplit (no partial sums to keep)
     const int esz = dtype_size(p.dtype);
     // Misaligned base pointers are staged too (the scratch is always there).
-    if (cfg.kernel != GEMM_KERNEL_SKINNY) {
+    if (cfg.kernel != GEMM_KERNEL_SKINNY && !ffma_small(cfg)) {
         if (reinterpret_cast<uintptr_t>(A) % 16 != 0) cfg.stage_a = 1;
         if (reinterpret_cast<uintptr_t>(B) % 16 != 0) cfg.stage_b = 1;
     }
@@ -219,6 +219,11 @@ extern "C" int gemm_run_noalloc(gemm_dtype_t dtype, int64_t M, int64_t N, int64_
         a.b_layout = ep.b_layout;
         return status_of(launch_skinny(cfg, a, s, e, lc));
     }
+    if (ffma_small(cfg))
+        return status_of(launch_ffma_small(static_cast<const float*>(A),
+                                           static_cast<const float*>(B), p.lda, p.ldb,
+                                           bt > 1 ? ep.stride_a : 0, bt > 1 ? ep.stride_b : 0,
+                                           ep.b_layout, s, e, st));
 
     const void* a_src = A;
     const void* b_src = B;

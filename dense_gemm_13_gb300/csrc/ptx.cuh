@@ -115,6 +115,15 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, bool p
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
+// Closes this thread's current group of cp.async copies.
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Waits until at most N of this thread's committed cp.async groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 // 3-D tiled store of one box from shared memory (bulk-group completion).
 // Out-of-range parts of the box are not written.

@@ -430,6 +430,82 @@ __global__ void __launch_bounds__(FTHREADS, (BN == 128 && !B_NK) ? 2 : 1)
     }
 }
 
+// Small problems (a few 128-row tiles would leave most SMs idle): 32 x 32
+// output tiles, one CTA of 256 threads each, the classic shared-memory tiling
+// of the pages ("SGEMM ... 83% of cuBLAS", sec. 3.1-3.4) with a 4-deep ring of
+// 32-deep K steps filled by 4-byte cp.async copies three steps ahead (as the
+// pages' cp.async double buffering, one step deeper).  The copies land A as
+// [k][m] and B as [k][n] (rows padded to 33 floats: conflict-free), each
+// thread keeps a 2 x 2 register tile (rows ty, ty + 16; columns tx, tx + 16).
+// Any stride and alignment of FP32 data; out-of-range elements arrive as zero.
+constexpr int SB = 32;   // tile rows, columns and K step
+constexpr int SST = 4;   // K steps in the ring
+__global__ void __launch_bounds__(256)
+    ffma_small_kernel(const float* __restrict__ A, const float* __restrict__ B, int64_t lda,
+                      int64_t ldb, int64_t stride_a, int64_t stride_b, int b_nk, int64_t M,
+                      int64_t N, int64_t K, const EpiParams e) {
+    __shared__ float As[SST][SB][SB + 1];
+    __shared__ float Bs[SST][SB][SB + 1];
+    const int tid = threadIdx.x;
+    const int64_t bz = blockIdx.z;
+    const int64_t m0 = static_cast<int64_t>(blockIdx.y) * SB, n0 = static_cast<int64_t>(blockIdx.x) * SB;
+    const float* Ab = A + bz * stride_a;
+    const float* Bb = B + bz * stride_b;
+    const int lr = tid >> 3, lc = (tid & 7) * 4;  // copier: row of the tile, 4 consecutive elements
+    const int ty = tid >> 4, tx = tid & 15;
+    const int64_t nsteps = (K + SB - 1) / SB;
+    // copies of K step `step` into ring slot step % SST (zero-filled out of range)
+    const auto issue = [&](int64_t step) {
+        const int sl = static_cast<int>(step % SST);
+        const int64_t k0 = step * SB;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int64_t m = m0 + lr, k = k0 + lc + q;
+            const bool in = m < M && k < K;
+            cp_async_4(smem_u32(&As[sl][lc + q][lr]), in ? Ab + m * lda + k : A, in);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (!b_nk) {  // B[k][n]: row k0 + lr, columns n0 + lc + q
+                const int64_t k = k0 + lr, n = n0 + lc + q;
+                const bool in = k < K && n < N;
+                cp_async_4(smem_u32(&Bs[sl][lr][lc + q]), in ? Bb + k * ldb + n : B, in);
+            } else {      // B[n][k]: row n0 + lr, columns k0 + lc + q
+                const int64_t n = n0 + lr, k = k0 + lc + q;
+                const bool in = n < N && k < K;
+                cp_async_4(smem_u32(&Bs[sl][lc + q][lr]), in ? Bb + n * ldb + k : B, in);
+            }
+        }
+    };
+    for (int st = 0; st < SST - 1; ++st) {
+        if (st < nsteps) issue(st);
+        cp_async_commit();
+    }
+    float acc[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
+    for (int64_t step = 0; step < nsteps; ++step) {
+        cp_async_wait_group<SST - 2>();  // this thread's copies of `step` have landed
+        __syncthreads();                 // everyone's have; everyone is done with step - 1
+        const int sl = static_cast<int>(step % SST);
+#pragma unroll
+        for (int kk = 0; kk < SB; ++kk) {
+            const float a0 = As[sl][kk][ty], a1 = As[sl][kk][ty + 16];
+            const float b0 = Bs[sl][kk][tx], b1 = Bs[sl][kk][tx + 16];
+            acc[0][0] = fmaf(a0, b0, acc[0][0]);
+            acc[0][1] = fmaf(a0, b1, acc[0][1]);
+            acc[1][0] = fmaf(a1, b0, acc[1][0]);
+            acc[1][1] = fmaf(a1, b1, acc[1][1]);
+        }
+        // refill the slot of step - 1 (every thread passed the barrier above after using it)
+        if (step + SST - 1 < nsteps) issue(step + SST - 1);
+        cp_async_commit();
+    }
+    cp_async_wait_all();
+    epi_store1(e, bz, m0 + ty, n0 + tx, acc[0][0]);
+    epi_store1(e, bz, m0 + ty, n0 + tx + 16, acc[0][1]);
+    epi_store1(e, bz, m0 + ty + 16, n0 + tx, acc[1][0]);
+    epi_store1(e, bz, m0 + ty + 16, n0 + tx + 16, acc[1][1]);
+}
+
 template <int BN, int STAGES, bool B_NK, bool PACKED>
 cudaError_t launch_ffma_t(const gemm_config_t& cfg, const CUtensorMap& tmA,
                           const CUtensorMap& tmB, const Shape& s, const EpiParams& e,
@@ -491,7 +567,21 @@ int max_ctas_t() {
 
 }  // namespace
 
+cudaError_t launch_ffma_small(const float* A, const float* B, int64_t lda, int64_t ldb,
+                              int64_t stride_a, int64_t stride_b, int b_layout, const Shape& s,
+                              const EpiParams& e, cudaStream_t stream) {
+    if (s.M <= 0 || s.N <= 0) return cudaSuccess;
+    const int64_t gx = (s.N + SB - 1) / SB, gy = (s.M + SB - 1) / SB;
+    if (gx >= (int64_t(1) << 31) || gy > 65535 || s.batch > 65535) return cudaErrorInvalidValue;
+    ffma_small_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy),
+                             static_cast<unsigned>(s.batch)),
+                        256, 0, stream>>>(A, B, lda, ldb, stride_a, stride_b,
+                                          b_layout == GEMM_B_NK ? 1 : 0, s.M, s.N, s.K, e);
+    return cudaGetLastError();
+}
+
 size_t ffma_smem_bytes(const gemm_config_t& cfg) {
+    if (cfg.variant == FFMA_VARIANT_SMALL) return 2 * SST * SB * (SB + 1) * sizeof(float);
     if (cfg.stages < 2 || cfg.stages > 4) return 0;
     if (cfg.bn == 128)
         return cfg.stages == 2   ? ffma_smem_total<128, 2>()
@@ -509,6 +599,8 @@ size_t ffma_partial_slot_bytes(const gemm_config_t& cfg) {
 }
 
 bool ffma_units_ok(const Shape& s, int bn) {
+    if (bn == SB)  // small-tile variant: grid (N/32, M/32, batch)
+        return (s.M + SB - 1) / SB <= 65535 && s.batch <= 65535;
     const int64_t units = ((s.M + FBM - 1) / FBM) * ((s.N + bn - 1) / bn) * s.batch *
                           ((s.K + FBK - 1) / FBK);
     return units < (int64_t(1) << 31);

@@ -129,7 +129,9 @@ typedef struct {
     int32_t stage_b;      /* 1: B likewise */
     int32_t num_ctas;     /* persistent grid size; 0 = one per SM */
     int32_t variant;      /* family-specific main-loop variant; FFMA: 0 scalar FFMA,
-                             1 packed fma.rn.f32x2 (KN layout only); TC: 0 single CTAs with
+                             1 packed fma.rn.f32x2 (KN layout only), 2 32 x 32 tiles from
+                             plain loads for small M x N (bm = bn = bk = 32, any stride or
+                             alignment, no stream-K); TC: 0 single CTAs with
                              4 epilogue warps, 1 single CTAs with 8 epilogue warps (short K),
                              2 CTA pairs (cta_group::2, 256 x 256 tiles, no split-K);
                              TF32X3: 0 single CTAs (bn 128), 2 CTA pairs (bn 256) */

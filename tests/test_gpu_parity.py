@@ -221,6 +221,29 @@ def test_ffma_variants_exact(bn, variant, stages, layout):
     assert run.guard_ok()
 
 
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+@pytest.mark.parametrize("shape", [(256, 256, 256), (33, 65, 31), (1, 40, 7), (200, 97, 1000)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_ffma_small_exact(shape, layout):
+    # 32 x 32 tiles from plain loads: ragged tiles and K steps, bit-exact on integers
+    w = _int_workload("f32", layout, *shape)
+    run = Run(w, config=g13.Config("ffma", 32, 32, 32, 2, variant=2))
+    C = run.run().result()
+    _, cref, _ = run.oracle()
+    assert np.array_equal(C, cref.reshape(C.shape)), f"{w.name}"
+    assert run.guard_ok()
+
+
+def test_ffma_small_epilogue_batched_unaligned():
+    # every epilogue step, a batch of 3, BF16 output and odd leading dimensions
+    # (plain loads: no staging copy, whatever the alignment)
+    w = Workload("ffma_small_epi", "f32", 70, 90, 45, batch=3, b_layout="nk", bias=True,
+                 act="gelu", residual=True, alpha=0.5, beta=0.25, out_dtype="bf16")
+    full_check(Run(w, config=g13.Config("ffma", 32, 32, 32, 2, variant=2), ldc_pad=1))
+    w2 = Workload("ffma_small_kn", "f32", 64, 48, 33, b_layout="kn", act="relu", residual=True)
+    full_check(Run(w2))  # the dispatcher's choice for a small FP32 problem
+
+
 @pytest.mark.parametrize("num_ctas", [0, 1, 3, 7, 50])
 @pytest.mark.parametrize("bn,variant,layout", [(128, 1, "kn"), (128, 0, "kn"), (128, 0, "nk"),
                                                (256, 1, "kn"), (256, 0, "kn")])

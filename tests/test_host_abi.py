@@ -111,7 +111,9 @@ def test_dispatch_buckets(lib):
     c = sel("f32", 8192, 8192, 8192)
     assert (c.bn, c.stream_k) == (256, 0)               # 2048 tiles = 13.5 waves: whole tiles
     c = sel("f32", 256, 256, 256)
-    assert (c.bn, c.stream_k) == (128, 1)
+    assert (c.bm, c.bn, c.variant, c.stream_k) == (32, 32, 2, 0)   # 4 tiles: small 32 x 32 tiles
+    c = sel("f32", 1024, 1024, 1024)
+    assert (c.bn, c.variant, c.stream_k) == (128, 1, 1)  # 64 tiles: stream-K
     assert sel("f32", 4096, 4096, 4096, "nk").variant == 0
     assert sel("f32", 256, 256, 256).kernel == "ffma"
     c = sel("bf16", 8192, 8192, 8192, "nk")
@@ -164,8 +166,10 @@ def test_dispatch_staging_follows_alignment(lib):
     assert (c.stage_a, c.stage_b) == (0, 1)
     c = sel("bf16", 1000, 1000, 6144, "kn")
     assert (c.stage_a, c.stage_b) == (0, 0)
-    c = sel("f32", 300, 300, 302)       # 302*4 B rows: not 16-B aligned
+    c = sel("f32", 3000, 3000, 302)     # 302*4 B rows: not 16-B aligned
     assert (c.kernel, c.stage_a, c.stage_b) == ("ffma", 1, 0)
+    c = sel("f32", 300, 300, 302)       # small: 32 x 32 tiles from plain loads, no staging
+    assert (c.kernel, c.variant, c.stage_a, c.stage_b) == ("ffma", 2, 0, 0)
 
 
 def test_dispatch_bn_by_waves(lib):
