@@ -818,29 +818,55 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                 // j of row r at r * 128 + ((j ^ (r & 7)) << 4), so row-wise
                 // (16-byte) and column-wise (4-byte) accesses are both free of bank
                 // conflicts.
-                uint8_t* sb = etile;
-                uint8_t* rowp = sb + lane * 128;
                 const uint32_t colx = ((lane >> 2) << 4) | ((lane & 3) << 2);  // column `lane`
                 const int rows_here =
                     static_cast<int>(max(int64_t(0), min(int64_t(32), e.M - row0)));
                 const bool smx = e.act == GEMM_ACT_SOFTMAX;  // v holds exp(t - max)
+                const bool any_r = !smx && !args.epi_plain && e.R != nullptr;
+                // The residual of a chunk goes out as asynchronous copies straight into
+                // the chunk's buffer (lane = column: 32 coalesced row segments, no
+                // registers held), one chunk ahead: chunk k uses buffer k & 1, and the
+                // copies for chunk k + 1 are issued when chunk k starts.
+                const auto r_copy = [&](uint8_t* dstb, int64_t bidx, int64_t r0, int64_t cgc,
+                                        int rows, int cols) {
+                    const float* rp = e.R + bidx * e.stride_r + r0 * e.ldr + cgc + lane;
+#pragma unroll
+                    for (int r = 0; r < 32; ++r) {
+                        const bool in = r < rows && lane < cols;
+                        cp_async_4(smem_u32(dstb + r * 128 + (colx ^ ((r & 7) << 4))),
+                                   in ? rp + r * e.ldr : e.R, in);
+                    }
+                    cp_async_commit();
+                };
 #pragma unroll 1
                 for (int c = c_lo; c < c_lo + SLICE; c += 32) {
                     const int64_t cg = col0 + c;
                     const int ncol = static_cast<int>(max(int64_t(0), min(int64_t(32), e.N - cg)));
-                    const bool with_r = ncol > 0 && !smx && !args.epi_plain && e.R;
-                    __syncwarp();  // the previous chunk's reads of the buffer are done
+                    const bool with_r = ncol > 0 && any_r;
+                    const int k = nchunk;
+                    uint8_t* sb = etile + (k & 1) * EPI_BUF_BYTES;
+                    uint8_t* rowp = sb + lane * 128;
+                    __syncwarp();  // the previous chunks' reads of both buffers are done
+                    bool ahead = false;
                     if (with_r) {
-                        // The residual goes out first, as asynchronous copies straight into
-                        // the buffer (lane = column: 32 coalesced row segments), so that
-                        // it overlaps the accumulator load and holds no registers.
-                        const float* rp =
-                            e.R + bt * e.stride_r + static_cast<int64_t>(row0) * e.ldr + cg + lane;
-#pragma unroll
-                        for (int r = 0; r < 32; ++r) {
-                            const bool in = r < rows_here && lane < ncol;
-                            cp_async_4(smem_u32(sb + r * 128 + (colx ^ ((r & 7) << 4))),
-                                       in ? rp + r * e.ldr : e.R, in);
+                        if (r_ahead != k) r_copy(sb, bt, row0, cg, rows_here, ncol);
+                        // next chunk: the rest of this tile, else this warp's first
+                        // chunk of its next work item (never split-K: no residual there)
+                        int64_t cn = cg + 32, rn = row0, bn = bt;
+                        bool has_next = c + 32 < c_lo + SLICE && cn < e.N;
+                        if (!has_next && t + item_stride < args.total_items) {
+                            int64_t mt2, nt2;
+                            tc_tile_coords(t + item_stride, args, bn, mt2, nt2);
+                            cn = nt2 * BN + c_lo;
+                            rn = mt2 * L::TILE_M + rank * TBM + q * 32;
+                            has_next = cn < e.N;
+                        }
+                        if (has_next) {
+                            r_copy(etile + ((k + 1) & 1) * EPI_BUF_BYTES, bn, rn, cn,
+                                   static_cast<int>(max(int64_t(0), min(int64_t(32), e.M - rn))),
+                                   static_cast<int>(min(int64_t(32), e.N - cn)));
+                            r_ahead = k + 1;
+                            ahead = true;
                         }
                     }
                     uint32_t v[32];
@@ -851,8 +877,13 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                         release(buf);
                     }
                     if (ncol == 0) continue;
+                    ++nchunk;
                     if (with_r) {
-                        cp_async_wait_all();
+                        // this chunk's copies (all but the newest group when one is ahead)
+                        if (ahead)
+                            cp_async_wait_group<1>();
+                        else
+                            cp_async_wait_all();
                         __syncwarp();
                     }
                     float y[32];
@@ -916,8 +947,9 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
         }
         // A residual load for a chunk that was never reached (the loop gave up)
         // must land before the CTA's shared memory goes away.
-        if (r_ahead >= nchunk && lane == 0)
+        if (args.epi_tma && r_ahead >= nchunk && lane == 0)
             tc_drain(smem_u32(&rb[r_ahead & 1]), (rph >> (r_ahead & 1)) & 1u, tmo);
+        cp_async_wait_all();
         // Shared memory must outlive the TMA stores that read it.
         if (lane == 0) bulk_wait_all();
         __syncwarp();
