@@ -688,28 +688,33 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
 #pragma unroll
                         for (int i = 0; i < W; ++i)
                             if (i < W) y[i] = __uint_as_float(v[i]) * sc;
+                    } else if (e.bias && args.bias_vec && cg + W <= e.N) {
+                        // alpha * acc + bias for pairs of columns: one packed FMA each
+                        const float* bp = e.bias + cg;
+                        const uint64_t a2 = f2_pack(e.alpha, e.alpha);
+#pragma unroll
+                        for (int i = 0; i < W; i += 4)
+                            if (i < W) {
+                                const float4 bv = __ldg(reinterpret_cast<const float4*>(bp + i));
+                                f2_unpack(f2_fma(f2_pack(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
+                                                 a2, f2_pack(bv.x, bv.y)),
+                                          y[i], y[i + 1]);
+                                f2_unpack(f2_fma(f2_pack(__uint_as_float(v[i + 2]), __uint_as_float(v[i + 3])),
+                                                 a2, f2_pack(bv.z, bv.w)),
+                                          y[i + 2], y[i + 3]);
+                            }
                     } else {
 #pragma unroll
                         for (int i = 0; i < W; ++i)
                             if (i < W) y[i] = __uint_as_float(v[i]) * e.alpha;
                         if (e.bias) {
                             const float* bp = e.bias + cg;
-                            if (args.bias_vec && cg + W <= e.N) {
 #pragma unroll
-                                for (int i = 0; i < W; i += 4)
-                                    if (i < W) {
-                                        const float4 bv = __ldg(reinterpret_cast<const float4*>(bp + i));
-                                        y[i] += bv.x;
-                                        y[i + 1] += bv.y;
-                                        y[i + 2] += bv.z;
-                                        y[i + 3] += bv.w;
-                                    }
-                            } else {
-#pragma unroll
-                                for (int i = 0; i < W; ++i)
-                                    if (i < W && cg + i < e.N) y[i] += __ldg(bp + i);
-                            }
+                            for (int i = 0; i < W; ++i)
+                                if (i < W && cg + i < e.N) y[i] += __ldg(bp + i);
                         }
+                    }
+                    if (!(args.epi_plain || smx)) {
                         if (e.act == GEMM_ACT_GELU_ERF) {
 #pragma unroll
                             for (int i = 0; i < W; i += 2) gelu2_as7126(y[i], y[i + 1]);
@@ -726,14 +731,15 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                                     return false;
                                 }
                                 rph ^= 1u << sel;
+                                const uint64_t b2 = f2_pack(e.beta, e.beta);
 #pragma unroll
                                 for (int j = 0; j < 8; ++j) {
                                     const float4 r4 =
                                         *reinterpret_cast<const float4*>(rowp + ((j ^ (lane & 7)) << 4));
-                                    y[4 * j] += e.beta * r4.x;
-                                    y[4 * j + 1] += e.beta * r4.y;
-                                    y[4 * j + 2] += e.beta * r4.z;
-                                    y[4 * j + 3] += e.beta * r4.w;
+                                    f2_unpack(f2_fma(f2_pack(r4.x, r4.y), b2, f2_pack(y[4 * j], y[4 * j + 1])),
+                                              y[4 * j], y[4 * j + 1]);
+                                    f2_unpack(f2_fma(f2_pack(r4.z, r4.w), b2, f2_pack(y[4 * j + 2], y[4 * j + 3])),
+                                              y[4 * j + 2], y[4 * j + 3]);
                                 }
                             } else if (row < e.M) {
                                 const float* rp = e.R + bt * e.stride_r + row * e.ldr + cg;
