@@ -178,6 +178,15 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------- GPU arm
+def workload_by_name(name: str):
+    """A named workload, or one triple of the ragged sweep as "sweep:M,N,K"."""
+    from dense_gemm_13_gb300.inputs import WORKLOADS, sweep_workload
+    if name.startswith("sweep:"):
+        M, N, K = (int(x) for x in name[len("sweep:"):].split(","))
+        return sweep_workload(M, N, K)
+    return WORKLOADS[name]
+
+
 def make_device_inputs(w, seed, device):
     t = w.make(seed)
     dev = {k: (v.to(device) if v is not None else None) for k, v in t.items()}
@@ -410,7 +419,7 @@ def run_ours(args):
 
     # "<workload>+3xtf32": the same FP32 workload with GEMM_FLAG_FP32_TENSOR
     base, _, mode = args.workload.partition("+")
-    w = WORKLOADS[base]
+    w = workload_by_name(base)
     host, dev = make_device_inputs(w, 0, device)
     plan = make_plan(g13, w, g13.FLAG_FP32_TENSOR if mode == "3xtf32" else 0)
     info = plan.info()
@@ -494,8 +503,8 @@ def run_reference(args):
         return
     import numpy as np
     import oracle
-    from dense_gemm_13_gb300.inputs import WORKLOADS, host_view
-    w = WORKLOADS[args.workload.partition("+")[0]]
+    from dense_gemm_13_gb300.inputs import host_view
+    w = workload_by_name(args.workload.partition("+")[0])
     host = w.make(0)
     A, B = host_view(host["A"]), host_view(host["B"])
     bias = host["bias"].numpy() if host["bias"] is not None else None
