@@ -140,6 +140,21 @@ def test_dispatch_buckets(lib):
     assert sel("bf16", 4096, 4096, 4096, flags=g13.FLAG_FP32_TENSOR).kernel == "tc"
 
 
+def test_dispatch_small_fp32(lib):
+    # 32 x 32 tiles from plain loads when the 128 x 128 tiles number at most one per
+    # eight SMs and K <= 512; otherwise the TMA-fed kernel (stream-K or whole tiles)
+    for M, N, K in ((256, 256, 256), (512, 512, 512), (300, 17, 100), (40, 9, 7)):
+        c = sel("f32", M, N, K)
+        assert (c.kernel, c.variant, c.bm, c.bn, c.stream_k) == ("ffma", 2, 32, 32, 0), (M, N, K)
+        assert (c.stage_a, c.stage_b) == (0, 0)
+    assert sel("f32", 512, 512, 1024).variant != 2           # longer K: stream-K splits K
+    assert sel("f32", 1024, 1024, 512).variant != 2          # 64 tiles > 152 / 8
+    assert sel("f32", 256, 256, 256, batch=96, stride_a=256 * 256, stride_b=256 * 256,
+               stride_c=256 * 256).variant != 2             # 384 tiles across the batch
+    assert sel("f32", 256, 256, 256, sms=8).variant != 2     # 4 tiles > 8 / 8
+    assert sel("bf16", 256, 256, 256).kernel == "tc"        # FP32 only
+
+
 def test_softmax_limits(lib):
     # the row softmax: tensor cores, one tile per row, 16-bit inputs only
     c = sel("bf16", 512, 512, 64, "nk", act="softmax")
