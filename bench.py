@@ -241,37 +241,87 @@ def time_device(g13, torch, w, plan, dev, steps, warmup, dist, device, C):
 
 
 def time_e2e(g13, torch, w, plan, host, steps, warmup, device):
-    """Same GEMM with host buffers: pinned H2D of the inputs, gemm_run, D2H of C, per step."""
+    """Same GEMM with host buffers: pinned H2D of the inputs, gemm_run, D2H of C, every step.
+
+    Two measurements.  Serial: one stream, each step's copies and GEMM back to back, the
+    median step.  Pipelined (the reported value): two sets of device buffers, a copy-in,
+    a compute and a copy-out stream ordered by events, so step i's copies overlap the
+    GEMMs of steps i - 1 and i + 1; whole-job time from the first copy-in to the last
+    copy-out, divided by the steps.  Every step still copies its own inputs in and its
+    result out inside the timed region.
+    """
     stream = torch.cuda.current_stream()
     hp = {k: (v.pin_memory() if v is not None else None) for k, v in host.items()}
-    dv = {k: (torch.empty_like(v, device=device) if v is not None else None) for k, v in host.items()}
     odt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[w.out_dtype]
     shape = (w.M, w.N) if w.batch == 1 else (w.batch, w.M, w.N)
-    C = torch.empty(shape, dtype=odt, device=device)
-    Ch = torch.empty(shape, dtype=odt).pin_memory()
+    slots = []
+    for _ in range(2):
+        dv = {k: (torch.empty_like(v, device=device) if v is not None else None)
+              for k, v in host.items()}
+        slots.append((dv, torch.empty(shape, dtype=odt, device=device),
+                      torch.empty(shape, dtype=odt).pin_memory()))
     h2d = sum(v.numel() * v.element_size() for v in hp.values() if v is not None)
-    d2h = Ch.numel() * Ch.element_size()
+    d2h = slots[0][2].numel() * slots[0][2].element_size()
 
-    def step():
-        for k, v in hp.items():
-            if v is not None:
-                dv[k].copy_(v, non_blocking=True)
-        g13.gemm_run(plan, dv["A"], dv["B"], C, dv["bias"], dv["R"], w.alpha)
-        Ch.copy_(C, non_blocking=True)
+    def step(slot, s_in, s_run, s_out, ev):
+        dv, C, Ch = slots[slot]
+        with torch.cuda.stream(s_in):
+            if ev is not None:
+                s_in.wait_event(ev["ran"][slot])      # the slot's inputs were consumed
+            for k, v in hp.items():
+                if v is not None:
+                    dv[k].copy_(v, non_blocking=True)
+            if ev is not None:
+                ev["in"][slot].record(s_in)
+        with torch.cuda.stream(s_run):
+            if ev is not None:
+                s_run.wait_event(ev["in"][slot])
+                s_run.wait_event(ev["out"][slot])     # the slot's C was read out
+            g13.gemm_run(plan, dv["A"], dv["B"], C, dv["bias"], dv["R"], w.alpha,
+                         stream=s_run.cuda_stream)
+            if ev is not None:
+                ev["ran"][slot].record(s_run)
+        with torch.cuda.stream(s_out):
+            if ev is not None:
+                s_out.wait_event(ev["ran"][slot])
+            Ch.copy_(C, non_blocking=True)
+            if ev is not None:
+                ev["out"][slot].record(s_out)
 
-    for _ in range(warmup):
-        step()
+    # serial: everything on the current stream
+    for i in range(warmup):
+        step(i % 2, stream, stream, stream, None)
     torch.cuda.synchronize()
     times = []
-    for _ in range(steps):
-        s = torch.cuda.Event(enable_timing=True)
-        e = torch.cuda.Event(enable_timing=True)
-        s.record(stream)
-        step()
-        e.record(stream)
-        e.synchronize()
-        times.append(s.elapsed_time(e))
-    return statistics.median(times), h2d, d2h
+    for i in range(steps):
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        step(i % 2, stream, stream, stream, None)
+        s1.record(stream)
+        s1.synchronize()
+        times.append(s0.elapsed_time(s1))
+    serial_ms = statistics.median(times)
+
+    # pipelined: copy-in, compute and copy-out streams
+    s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "ran", "out")}
+    for e_list in ev.values():
+        for e in e_list:
+            e.record(stream)
+    torch.cuda.synchronize()
+    for i in range(warmup):
+        step(i % 2, s_in, s_run, s_out, ev)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(s_in)
+    for i in range(steps):
+        step(i % 2, s_in, s_run, s_out, ev)
+    t1.record(s_out)
+    torch.cuda.synchronize()
+    pipe_ms = t0.elapsed_time(t1) / steps
+    return pipe_ms, serial_ms, h2d, d2h
 
 
 def roofline_for(w, kernel, ms, pk, pk_kind):
@@ -457,11 +507,17 @@ def run_ours(args):
     if cs:
         result["clocks"] = cs
     if not args.no_e2e:
-        e2e_ms, h2d, d2h = time_e2e(g13, torch, w, plan, host, max(10, args.steps // 5), 3, device)
+        e2e_ms, serial_ms, h2d, d2h = time_e2e(g13, torch, w, plan, host, max(10, args.steps // 5),
+                                               3, device)
         result["e2e"] = {"value": round(w.flops * ws / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOPS",
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                          "ms_per_step": round(e2e_ms, 4),
-                         "how": "pinned host inputs copied in, gemm_run, C copied out; median"}
+                         "serial_ms_per_step": round(serial_ms, 4),
+                         "serial_value": round(w.flops * ws / (serial_ms * 1e-3) / 1e12, 3),
+                         "how": "every step copies its pinned host inputs in, runs gemm_run and "
+                                "copies C out; value: two buffer sets on copy-in / compute / "
+                                "copy-out streams, whole-job time / steps; serial: one stream, "
+                                "median step"}
     if not args.no_extra:
         extra = []
         for name in ("bf16_8192", "bf16_4096", "ffn1_bf16", "ffn1_f16", "ffn2_bf16", "qkt_bf16",
