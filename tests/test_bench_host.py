@@ -85,3 +85,11 @@ def test_recorded_traffic_follows_the_source_hash(tmp_path):
     assert bench.recorded_traffic("ffma", "sgemm_4096", root) == 1234.0
     assert bench.recorded_traffic("tc", "bf16_8192", root) is None          # stale hash
     assert bench.recorded_traffic("ffma", "no_such_workload", root) is None
+
+
+def test_workload_names_include_sweep_triples():
+    w = bench.workload_by_name("sweep:3001,17,4097")
+    assert (w.M, w.N, w.K, w.dtype, w.residual, w.alpha) == (3001, 17, 4097, "bf16", True, 0.5)
+    assert bench.workload_by_name("ffn2_bf16") is WORKLOADS["ffn2_bf16"]
+    with pytest.raises(KeyError):
+        bench.workload_by_name("no_such_workload")
