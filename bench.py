@@ -23,7 +23,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -109,16 +108,16 @@ def source_hash(kernel: str) -> str:
 
 
 def recorded_traffic(kernel: str, workload: str, root: str = ROOT):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged since."""
-    path = os.path.join(root, "profiles", f"ncu_{kernel}_{workload}.md")
+    """DRAM bytes per launch recorded from an ncu capture (profiles/traffic.json), if the
+    kernel's sources still hash the same as when the counters were taken, else None."""
+    path = os.path.join(root, "profiles", "traffic.json")
     if not os.path.exists(path) or kernel not in KERNEL_SOURCES:
         return None
-    txt = open(path).read()
-    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
-    hsh = re.search(r"source_hash:\s*([0-9a-f]+)", txt)
-    if not m or not hsh or hsh.group(1) != source_hash(kernel):
+    with open(path) as f:
+        rec = json.load(f).get(f"{kernel}/{workload}")
+    if not rec or rec.get("source_hash") != source_hash(kernel):
         return None
-    return float(m.group(1))
+    return float(rec["dram_bytes_per_launch"])
 
 
 class ClockSampler:
@@ -324,11 +323,12 @@ def time_e2e(g13, torch, w, plan, host, steps, warmup, device):
     return pipe_ms, serial_ms, h2d, d2h
 
 
-def roofline_for(w, kernel, ms, pk, pk_kind):
-    """Roofline object for the workload's main kernel (achieved from the median launch)."""
+def roofline_for(w, kernel, ms, pk, pk_kind, num_sms=152):
+    """Roofline object for the workload's main kernel (achieved from the median launch).
+    num_sms: the SMs of the plan's device (the FP32 FMA peak scales with it)."""
     flops = w.flops
     if kernel == "ffma":
-        sm_count = 152
+        sm_count = num_sms
         peak = sm_count * FP32_LANES_PER_SM * 2 * pk.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
         return {"bound": "alu", "achieved": flops / (ms * 1e-3) / 1e12, "peak": round(peak, 2),
                 "unit": "TFLOP/s", "peak_source": f"derived: {sm_count} SMs x {FP32_LANES_PER_SM} FP32 "
@@ -339,7 +339,8 @@ def roofline_for(w, kernel, ms, pk, pk_kind):
         peak = pk["bf16_tflops"] * TF32_PER_BF16
         return {"bound": "tensor", "achieved": 3 * flops / (ms * 1e-3) / 1e12,
                 "peak": round(peak, 1), "unit": "TFLOP/s (TF32 MMA work, 3 x 2MNK)",
-                "peak_source": f"{pk_kind} bf16_tflops x {TF32_PER_BF16:.3f} (nominal TF32/BF16)"}
+                "peak_source": f"{pk_kind} bf16_tflops x {TF32_PER_BF16:.3f} (nominal TF32/BF16)",
+                "frac_basis": "against a nominal ratio: no TF32 peak is measured on this GPU"}
     byts = w.algorithmic_bytes()
     ai = flops / byts
     bw = pk["hbm_gbs"] * 1e9
@@ -394,7 +395,7 @@ def sweep_summary(g13, torch, device, pk, pk_kind, reps=8):
                         ts.append((s0, s1))
                 torch.cuda.synchronize()
                 ms = statistics.median(a.elapsed_time(b) for a, b in ts)
-                r = roofline_for(w, kern, ms, pk, pk_kind)
+                r = roofline_for(w, kern, ms, pk, pk_kind, plan.info()["num_sms"])
                 if kern == "skinny" or min(M, N) <= 16:
                     bucket = "skinny"
                 elif r["bound"] == "hbm":
@@ -496,7 +497,7 @@ def run_ours(args):
                    "kernel": info["config"].as_dict(), "l2": "flushed between steps (512 MiB write)",
                    "timing": "per-step CUDA events, median", "parallelism": f"replicas x{ws}"},
     }
-    rf = roofline_for(w, kernel, mean, pk, pk_kind)
+    rf = roofline_for(w, kernel, mean, pk, pk_kind, info["num_sms"])
     rf["achieved"] = round(rf["achieved"], 3)
     rf["frac"] = round(rf["achieved"] / rf["peak"], 4)
     rf["timed_on"] = "mean launch duration over the timed steps"
@@ -535,7 +536,7 @@ def run_ours(args):
             tx = max_over_ranks(tx, dist, device)
             mx = statistics.median(tx)
             kx = px.info()["config"].kernel
-            r = roofline_for(wx, kx, statistics.fmean(tx), pk, pk_kind)
+            r = roofline_for(wx, kx, statistics.fmean(tx), pk, pk_kind, px.info()["num_sms"])
             extra.append({"workload": name, "tflops": round(wx.flops / (mx * 1e-3) / 1e12, 2),
                           "ms": round(mx, 4), "kernel": kx, "bn": px.info()["config"].bn,
                           "bound": r["bound"], "frac": round(r["achieved"] / r["peak"], 4)})

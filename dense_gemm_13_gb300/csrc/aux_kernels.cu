@@ -493,6 +493,44 @@ __global__ void __launch_bounds__(256) split_reduce_kernel(const float* __restri
 
 }  // namespace
 
+namespace {
+template <typename T, int PM>
+cudaError_t skinny_attr_t() {
+    cudaFuncAttributes fa;
+    cudaError_t err = cudaFuncGetAttributes(&fa, skinny_dot_kernel<T, PM, false>);
+    if (err == cudaSuccess) err = cudaFuncGetAttributes(&fa, skinny_dot_kernel<T, PM, true>);
+    if (err == cudaSuccess) err = cudaFuncGetAttributes(&fa, skinny_axpy_kernel<T, PM>);
+    return err;
+}
+template <typename T>
+cudaError_t skinny_attr_pm() {
+    cudaError_t err = skinny_attr_t<T, 1>();
+    if (err == cudaSuccess) err = skinny_attr_t<T, 4>();
+    if (err == cudaSuccess) err = skinny_attr_t<T, 16>();
+    return err;
+}
+// SMs of the launch's device: the plan's count, else the current device's.
+int launch_sms(const LaunchCtx& lc) {
+    if (lc.num_sms > 0) return lc.num_sms;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0)
+        return sms;
+    return 1;
+}
+
+}  // namespace
+
+cudaError_t aux_preload_kernels() {
+    // A function-attribute query makes the runtime load a lazily loaded kernel.
+    cudaFuncAttributes fa;
+    cudaError_t err = cudaFuncGetAttributes(&fa, stage_copy_kernel);
+    if (err == cudaSuccess) err = skinny_attr_pm<float>();
+    if (err == cudaSuccess) err = skinny_attr_pm<__half>();
+    if (err == cudaSuccess) err = skinny_attr_pm<__nv_bfloat16>();
+    return err;
+}
+
 cudaError_t launch_stage_copy(const void* src, int64_t rows, int64_t cols, int64_t ld,
                               int64_t bstride, int64_t batch, int esz, void* dst, int64_t dst_ld,
                               cudaStream_t stream) {
@@ -567,7 +605,7 @@ cudaError_t launch_skinny(const gemm_config_t& cfg, const SkinnyArgs& a, const S
     sp.l_vec = al16(sp.L, sp.ldl, sp.stride_l, s.batch, esz) ? 1 : 0;
     sp.s_vec = (sp.s_sk == 1 && al16(sp.S, sp.s_sp, sp.stride_s, s.batch, esz)) ? 1 : 0;
     sp.e = e;
-    const int sms = lc.num_sms > 0 ? lc.num_sms : 148;
+    const int sms = launch_sms(lc);
     const int pm = sp.P == 1 ? 1 : sp.P <= 4 ? 4 : 16;
     if (dot) {
         const int64_t items = s.batch * sp.Q * sp.splits;
@@ -755,7 +793,7 @@ cudaError_t launch_split_reduce(const float* partial, int64_t M, int64_t N, int6
                                 int splits, const EpiParams& e, const LaunchCtx& lc) {
     const int64_t quads = batch * M * ((N + 3) / 4);
     if (quads <= 0) return cudaSuccess;
-    const int sms = lc.num_sms > 0 ? lc.num_sms : 148;
+    const int sms = launch_sms(lc);
     if (splits > 8 && quads < static_cast<int64_t>(sms) * 64) {
         const int64_t outs = batch * M * N;
         int64_t rb = (outs + 31) / 32;

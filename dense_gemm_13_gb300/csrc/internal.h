@@ -138,4 +138,11 @@ cudaError_t launch_stage_copy(const void* src, int64_t rows, int64_t cols, int64
                               int64_t bstride, int64_t batch, int esz, void* dst,
                               int64_t dst_ld, cudaStream_t stream);
 
+// Load every kernel the allocation-free entry point can launch onto the
+// current device (under lazy module loading a kernel is otherwise loaded, and
+// its device memory allocated, at its first launch).
+cudaError_t tc_preload_kernels();
+cudaError_t ffma_preload_kernels();
+cudaError_t aux_preload_kernels();
+
 }  // namespace g13

@@ -19,12 +19,18 @@
 //   * calls whose kernels overlap on the GPU (different streams, or several
 //     host threads) race on the array: order them on one stream, or use
 //     gemm_plan / gemm_run instead;
-//   * device-side wait timeouts are recorded in the shared status word but are
-//     not reported to the caller (there is no plan to query).
-// Set-up: the first call on each device, with that device current, looks up
-// the array's device address with cudaGetSymbolAddress; make that first call
-// before any stream capture.  Problems whose staged operands need more than
-// kScratchBytes return GEMM_ERR_SCRATCH_LIMIT.
+//   * a device-side wait that runs out (default limit 2 s per wait) makes the
+//     kernels give up: C is then undefined (partly written).  The condition is
+//     recorded in the shared status word but not reported to the caller
+//     (there is no plan to query); use gemm_plan / gemm_run where it matters.
+// Set-up: the first call on each device and CUDA context (with that device
+// current) looks up the array's device address with cudaGetSymbolAddress and
+// loads every kernel this entry point can launch.  Under CUDA's lazy module
+// loading both steps allocate device memory inside the CUDA driver, so make
+// that first call before the region that must not allocate, and before any
+// stream capture; a call with M = 0 or N = 0 does the set-up and nothing else.
+// Problems whose staged operands need more than kScratchBytes return
+// GEMM_ERR_SCRATCH_LIMIT.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -48,21 +54,54 @@ static __device__ __align__(256) unsigned char g13_noalloc_scratch[kScratchBytes
 namespace {
 
 std::mutex g_setup_mu;
+// Per device: the context the set-up ran in and the array's address there.
+// A different current context (a non-primary one, or the primary one after a
+// device reset) gets its own set-up.
+CUcontext g_setup_ctx[kMaxDevices] = {};
 void* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of this device's scratch array (looked up once per device).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current_fn() {
+    static CtxGetCurrentFn fn = []() -> CtxGetCurrentFn {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<CtxGetCurrentFn>(p);
+    }();
+    return fn;
+}
+
+// Device address of the scratch array in the current device's current
+// context; the first call there also loads the kernels this entry point uses.
 int scratch_for_current_device(void** out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return GEMM_ERR_NO_DEVICE;
+    CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+    if (!get_ctx) return GEMM_ERR_NO_DEVICE;
+    // Null before the runtime has made a context current on this thread.
+    CUcontext ctx = nullptr;
+    if (get_ctx(&ctx) != CUDA_SUCCESS) return GEMM_ERR_NO_DEVICE;
     std::lock_guard<std::mutex> lk(g_setup_mu);
-    if (!g_scratch_ptr[dev]) {
+    if (!ctx || !g_scratch_ptr[dev] || g_setup_ctx[dev] != ctx) {
         void* p = nullptr;
+        // (binds the device's primary context if none is current)
         if (cudaGetSymbolAddress(&p, g13_noalloc_scratch) != cudaSuccess || !p) {
             cudaGetLastError();
             return GEMM_ERR_CUDA;
         }
+        if (g13::tc_preload_kernels() != cudaSuccess || g13::ffma_preload_kernels() != cudaSuccess ||
+            g13::aux_preload_kernels() != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        if (get_ctx(&ctx) != CUDA_SUCCESS || !ctx) return GEMM_ERR_NO_DEVICE;
         g_scratch_ptr[dev] = p;
+        g_setup_ctx[dev] = ctx;
     }
     *out = g_scratch_ptr[dev];
     return GEMM_OK;
@@ -130,11 +169,6 @@ extern "C" int gemm_run_noalloc(gemm_dtype_t dtype, int64_t M, int64_t N, int64_
     int rc = make_problem(dtype, M, N, K, lda, ldb, ldc, epilogue, &p);
     if (rc != GEMM_OK) return rc;
     const gemm_epilogue_t& ep = p.epi;
-    if (p.M == 0 || p.N == 0) return GEMM_OK;
-    if (!C) return GEMM_ERR_INVALID_ARG;
-    if (p.K > 0 && (!A || !B)) return GEMM_ERR_INVALID_ARG;
-    if ((ep.has_bias != 0) != (bias != nullptr)) return GEMM_ERR_INVALID_ARG;
-    if ((ep.has_residual != 0) != (residual != nullptr)) return GEMM_ERR_INVALID_ARG;
 
     int dev = -1, major = 0, minor = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -143,6 +177,16 @@ extern "C" int gemm_run_noalloc(gemm_dtype_t dtype, int64_t M, int64_t N, int64_
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return GEMM_ERR_NO_DEVICE;
     if (major != 10 || minor != 3) return GEMM_ERR_NO_DEVICE;
+    // Set-up (first call per device and context), also for empty problems.
+    void* scratch = nullptr;
+    rc = scratch_for_current_device(&scratch);
+    if (rc != GEMM_OK) return rc;
+
+    if (p.M == 0 || p.N == 0) return GEMM_OK;
+    if (!C) return GEMM_ERR_INVALID_ARG;
+    if (p.K > 0 && (!A || !B)) return GEMM_ERR_INVALID_ARG;
+    if ((ep.has_bias != 0) != (bias != nullptr)) return GEMM_ERR_INVALID_ARG;
+    if ((ep.has_residual != 0) != (residual != nullptr)) return GEMM_ERR_INVALID_ARG;
 
     gemm_config_t cfg;
     p.epi.flags &= ~GEMM_FLAG_FP32_TENSOR;  // 3xTF32 needs split buffers: FP32 runs on FFMA
@@ -170,9 +214,6 @@ extern "C" int gemm_run_noalloc(gemm_dtype_t dtype, int64_t M, int64_t N, int64_
     const size_t b_bytes = cfg.stage_b ? static_cast<size_t>(round_up(b_bat * b_rows * ldb_s * esz, 256)) : 0;
     if (kStatusBytes + a_bytes + b_bytes > kScratchBytes) return GEMM_ERR_SCRATCH_LIMIT;
 
-    void* scratch = nullptr;
-    rc = scratch_for_current_device(&scratch);
-    if (rc != GEMM_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     unsigned* status = static_cast<unsigned*>(scratch);
     cudaError_t ce = cudaMemsetAsync(status, 0, sizeof(unsigned), st);

@@ -649,6 +649,37 @@ cudaError_t launch_ffma(const gemm_config_t& cfg, int b_layout, const CUtensorMa
     return cudaErrorInvalidValue;
 }
 
+template <int BN, int ST, bool NK, bool PK>
+cudaError_t ffma_attr_t() {
+    cudaFuncAttributes fa;
+    return cudaFuncGetAttributes(&fa, ffma_kernel<BN, ST, NK, PK>);
+}
+
+static cudaError_t ffma_preload_one(const gemm_config_t& cfg, int b_layout) {
+#define G13_ATTR(BN, ST, NK, PK) ffma_attr_t<BN, ST, NK, PK>()
+    G13_FFMA_DISPATCH(G13_ATTR)
+#undef G13_ATTR
+    return cudaSuccess;
+}
+
+cudaError_t ffma_preload_kernels() {
+    // A function-attribute query makes the runtime load a lazily loaded kernel.
+    cudaFuncAttributes fa;
+    cudaError_t err = cudaFuncGetAttributes(&fa, ffma_small_kernel);
+    for (int bn = 128; bn <= 256 && err == cudaSuccess; bn += 128)
+        for (int st = 2; st <= 4 && err == cudaSuccess; ++st)
+            for (int var = 0; var <= 1 && err == cudaSuccess; ++var)
+                for (int lay = GEMM_B_KN; lay <= GEMM_B_NK && err == cudaSuccess; ++lay) {
+                    gemm_config_t cfg{};
+                    cfg.kernel = GEMM_KERNEL_FFMA;
+                    cfg.bn = bn;
+                    cfg.stages = st;
+                    cfg.variant = var;
+                    err = ffma_preload_one(cfg, lay);
+                }
+    return err;
+}
+
 #undef G13_FFMA_DISPATCH
 
 }  // namespace g13

@@ -1154,6 +1154,20 @@ cudaError_t launch_tc(const gemm_config_t& cfg, int dtype, int b_layout, const C
     return launch_tc_layout<false>(cfg, dtype, tmA, tmB, em, s, e, lc, final_epi);
 }
 
+cudaError_t tc_preload_kernels() {
+    // A function-attribute query makes the runtime load a lazily loaded kernel.
+    cudaFuncAttributes fa;
+    cudaError_t err = cudaSuccess;
+#define G13_TC_PRELOAD(BN, ST, EW, VAR, PAIR)                                                   \
+    if (err == cudaSuccess)                                                                     \
+        err = cudaFuncGetAttributes(&fa, tc_gemm_kernel<BN, ST, true, EW, PAIR, false>);        \
+    if (err == cudaSuccess)                                                                     \
+        err = cudaFuncGetAttributes(&fa, tc_gemm_kernel<BN, ST, false, EW, PAIR, false>);
+    G13_TC_CONFIGS(G13_TC_PRELOAD)
+#undef G13_TC_PRELOAD
+    return err;
+}
+
 #undef G13_TC_CONFIGS
 #undef G13_TC3_CONFIGS
 

@@ -225,7 +225,8 @@ const char* gemm_version(void);
 
 /*
  * gemm_run_noalloc -- the same GEMM as gemm_plan + gemm_run in one call that
- * allocates no memory at all (no cudaMalloc, no plan, no host heap).  The
+ * allocates no memory (no cudaMalloc, no plan, no host heap) once its
+ * per-device set-up (below) has run.  The
  * pages have no counterpart: this exists for callers that cannot allocate
  * device memory where they run a GEMM -- code inside an allocator or memory-
  * pool callback, code holding a lock the allocator also takes, or programs
@@ -237,7 +238,7 @@ const char* gemm_version(void);
  *
  * Scratch: operands that TMA cannot read in place (strides or base addresses
  * not 16-byte aligned) are copied into a fixed 64 MiB device array inside the
- * library, one per GPU, resident from library load until process exit.  The
+ * library, one per GPU, resident from the set-up until process exit.  The
  * array also holds the status word.  If the staged copies need more than
  * that (each staged row padded to 16 bytes, 256 bytes reserved), the call
  * returns GEMM_ERR_SCRATCH_LIMIT and does nothing.
@@ -245,11 +246,19 @@ const char* gemm_version(void);
  * Sharing: every call on a device uses the same array and finds the previous
  * call's data in it (it rewrites what it uses).  Calls whose work overlaps on
  * the GPU -- on different streams or from several threads -- race on the
- * array; order them on one stream.  Device-side wait timeouts are not
- * reported by this call.
+ * array; order them on one stream.
  *
- * Set-up: the first call on each device (with that device current) looks up
- * the array's device address; make that first call before any stream capture.
+ * Device timeouts: if a kernel gives up on a device-side wait (default limit
+ * 2 s per wait), C is left undefined (partly written).  This call cannot
+ * report that (there is no plan whose status could be queried); callers that
+ * need to know use gemm_plan / gemm_run / gemm_plan_status.
+ *
+ * Set-up: the first call on each device and CUDA context (with that device
+ * current) looks up the array's device address and loads every kernel this
+ * entry point can launch.  Under CUDA's lazy module loading both steps make
+ * the CUDA driver allocate device memory, so make that first call before the
+ * code that must not allocate, and before any stream capture.  A call with
+ * M = 0 or N = 0 performs the set-up and nothing else.
  *
  * Errors: INVALID_ARG, UNSUPPORTED, SCRATCH_LIMIT, NO_DEVICE, CUDA.
  */

@@ -151,7 +151,12 @@ class Run:
         return float(np.max(err / np.maximum(tol, 1e-300))) if err.size else 0.0
 
     def freivalds(self, C: np.ndarray, trials: int = 2, seed: int = 99):
-        """Whole-matrix check for linear epilogues: |C x - v| <= sum_j |x_j| tol_ij."""
+        """Whole-matrix check for linear epilogues: |C x - v| <= sum_j |x_j| tol_ij.
+
+        This catches NaNs, Infs and gross errors anywhere in C, not a wrong
+        tile: at large K the bound on a row sum is far wider than what one
+        128 x 256 tile of wrong values moves it by.  Tile coverage comes from
+        the element-wise checks on `tile_indices` rows and columns."""
         w, t = self.w, self.t
         assert w.act == "none"
         rng = np.random.default_rng(seed)
@@ -180,3 +185,18 @@ def boundary_indices(n: int, tiles=(64, 128, 256), extra: int = 6, seed: int = 5
     rng = np.random.default_rng(seed + n)
     s.update(int(v) for v in rng.integers(0, max(n, 1), extra))
     return np.array(sorted(v for v in s if 0 <= v < n), dtype=np.int64)
+
+
+def tile_indices(n: int, block: int = 128, seed: int = 7) -> np.ndarray:
+    """The tile-edge indices of `boundary_indices` plus one index at a random
+    offset inside every `block`-wide block of [0, n).
+
+    Checking every column of these rows (and every row of these columns)
+    element by element reaches every output tile of any tiling whose tile
+    sides are multiples of `block` (128 x 128, 128 x 256, 256 x 256 CTA-pair
+    tiles, the raster-group wraps and the later persistent waves alike)."""
+    s = set(int(v) for v in boundary_indices(n, extra=4, seed=seed))
+    rng = np.random.default_rng(seed * 7919 + n)
+    for b0 in range(0, n, block):
+        s.add(b0 + int(rng.integers(0, min(block, n - b0))))
+    return np.array(sorted(s), dtype=np.int64)

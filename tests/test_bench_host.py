@@ -3,6 +3,7 @@ world-size-2 process group (gloo on CPU, rendezvous on 127.0.0.1), the
 reference arm's rank handling, and the roofline / traffic bookkeeping."""
 import os
 import socket
+import json
 import types
 
 import pytest
@@ -78,13 +79,19 @@ def test_roofline_bounds_and_peaks():
 def test_recorded_traffic_follows_the_source_hash(tmp_path):
     prof = tmp_path / "profiles"
     prof.mkdir()
-    (prof / "ncu_ffma_sgemm_4096.md").write_text(
-        f"dram_bytes_per_launch: 1234\nsource_hash: {bench.source_hash('ffma')}\n")
-    (prof / "ncu_tc_bf16_8192.md").write_text("dram_bytes_per_launch: 99\nsource_hash: 0000\n")
+    (prof / "traffic.json").write_text(json.dumps({
+        "ffma/sgemm_4096": {"dram_bytes_per_launch": 1234, "source_hash": bench.source_hash("ffma")},
+        "tc/bf16_8192": {"dram_bytes_per_launch": 99, "source_hash": "0000"}}))
     root = str(tmp_path)
     assert bench.recorded_traffic("ffma", "sgemm_4096", root) == 1234.0
     assert bench.recorded_traffic("tc", "bf16_8192", root) is None          # stale hash
     assert bench.recorded_traffic("ffma", "no_such_workload", root) is None
+
+
+def test_fp32_peak_follows_the_plan_sm_count():
+    pk = {"hbm_gbs": 6790.7, "bf16_tflops": 1912.4, "sm_max_mhz": 2070.0}
+    r = bench.roofline_for(WORKLOADS["sgemm_4096"], "ffma", 2.5, pk, "measured", num_sms=148)
+    assert abs(r["peak"] - 148 * 128 * 2 * 2.07e9 / 1e12) < 0.01 and "148 SMs" in r["peak_source"]
 
 
 def test_workload_names_include_sweep_triples():

@@ -1,8 +1,11 @@
 """GPU parity: the library (through the C ABI) against the FP64 oracle.
 
-Small problems are compared element by element in full; the full-size
-workloads on tile-boundary rows/columns (every column of the sampled rows and
-every row of the sampled columns) plus a Freivalds whole-matrix check.
+Small problems are compared element by element in full.  The full-size
+workloads are compared element by element on every column of a set of rows
+and every row of a set of columns: the tile-edge rows and columns plus one at
+a random offset inside every 128-wide block, so every output tile (and every
+raster-group wrap and persistent wave) has checked elements; a Freivalds
+whole-matrix check adds a test for NaNs and gross errors.
 Every run also checks the NaN guard bands around C.
 """
 import itertools
@@ -13,7 +16,7 @@ import torch
 
 import dense_gemm_13_gb300 as g13
 from dense_gemm_13_gb300.inputs import WORKLOADS, Workload, matrix
-from tests.gpu_check import Run, boundary_indices
+from tests.gpu_check import Run, tile_indices
 
 pytestmark = pytest.mark.gpu
 
@@ -170,7 +173,8 @@ def test_tf32x3_chosen_with_flag_at_4096():
     run = Run(w, flags=g13.FLAG_FP32_TENSOR)
     assert run.info["config"].kernel == "tf32x3"
     C = run.run().result()
-    run.check(C, rows=boundary_indices(w.M), cols=boundary_indices(w.N))
+    run.check(C, rows=tile_indices(w.M), label=" [rows]")
+    run.check(C, cols=tile_indices(w.N), label=" [cols]")
     run.freivalds(C)
     assert Run(w, tensors=run.t).info["config"].kernel == "ffma"   # without the flag: FFMA
 
@@ -438,10 +442,12 @@ def test_workload_sampled(name):
     w = WORKLOADS[name]
     run = Run(w)
     C = run.run().result()
-    rows = boundary_indices(w.M, extra=4)
-    cols = boundary_indices(w.N, extra=4)
-    run.check(C, rows=rows, label=" [sampled rows]")
-    run.check(C, cols=cols, label=" [sampled cols]")
+    rows = tile_indices(w.M)
+    cols = tile_indices(w.N)
+    assert len(np.unique(rows // 128)) == (w.M + 127) // 128
+    assert len(np.unique(cols // 128)) == (w.N + 127) // 128
+    run.check(C, rows=rows, label=" [rows: one per 128-row block]")
+    run.check(C, cols=cols, label=" [cols: one per 128-column block]")
     if w.act == "none" and w.out_dtype == "f32":
         run.freivalds(C)
     assert run.guard_ok()
