@@ -29,6 +29,7 @@ KERNELS = {"auto": 0, "tc": 1, "ffma": 2, "skinny": 3, "tf32x3": 4}
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 FLAG_FP32_TENSOR = 0x1         # FP32 inputs may run as 3xTF32 on the tensor cores
 FLAG_TEST_STALL = 0x80000000
+FLAG_TEST_STALL_PEER = 0x40000000   # test only: the second CTA withholds a tile
 
 STATUS = {0: "GEMM_OK", -1: "GEMM_ERR_INVALID_ARG", -2: "GEMM_ERR_UNSUPPORTED",
           -3: "GEMM_ERR_MISALIGNED", -4: "GEMM_ERR_CUDA", -5: "GEMM_ERR_DEVICE_TIMEOUT",

@@ -174,9 +174,10 @@ template <int BN, int STAGES, int EW, bool PAIR, bool K3>
 __host__ __device__ constexpr int tc_smem_total() {
     // ring + epilogue tiles + full/empty per stage + tfull/tempty x2 + drain
     // + residual barriers (2 per epilogue warp) + softmax exchange barriers (4)
-    // + tmem slot + abort flag + softmax exchange values [2][EW][32] floats
-    return 1024 + tc_bar_off<BN, STAGES, EW, PAIR, K3>() + (2 * STAGES + 9 + 2 * EW) * 8 + 16 +
-           2 * EW * 32 * 4;
+    // + pair exit barriers (2) + per-stage copy counts (8) + tmem slot + abort
+    // flag + softmax exchange values [2][EW][32] floats
+    return 1024 + tc_bar_off<BN, STAGES, EW, PAIR, K3>() + (2 * STAGES + 11 + 2 * EW) * 8 + 32 +
+           16 + 2 * EW * 32 * 4;
 }
 
 // 32-bit arithmetic: the host keeps the tile count below 2^31.
@@ -203,6 +204,35 @@ __device__ __forceinline__ void tc_drain(uint32_t bar, uint32_t parity, uint64_t
         if (globaltimer_ns() - t0 > timeout_ns) return;
 }
 
+// Pair exit: waits, with acquire at cluster scope, for a phase of a local
+// barrier that the peer CTA arrives on; false after limit_ns.
+__device__ __forceinline__ bool mbar_wait_peer(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+// 32-bit load from the shared memory of a CTA of the cluster (a mapa address).
+__device__ __forceinline__ uint32_t ld_peer_u32(uint32_t cluster_addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+// Counts `bytes` as arrived on a local barrier's current phase without a copy.
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
 template <int BN, int STAGES, bool B_KN, int EW, bool PAIR, bool K3>
 __global__ void __launch_bounds__(tc_threads<EW>(), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -210,6 +240,7 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                    const TcArgs args) {
     using L = TcLayout<BN, PAIR, K3>;
     static_assert(!(K3 && B_KN), "3xTF32 reads B K-major (the split pass transposes KN)");
+    static_assert(STAGES <= 8, "per-stage copy counts hold 8 stages");
     // Accumulator buffers in TMEM: two of BN columns, or one for 512-wide
     // tiles (the row softmax), which fill all 512 columns.
     constexpr int NBUF = BN > 256 ? 1 : 2;
@@ -225,7 +256,10 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
     uint64_t* drain = tempty + 2;
     uint64_t* rbar = drain + 1;  // [EW][2] residual-chunk barriers
     uint64_t* xbar = rbar + 2 * EW;  // [4] softmax: the two warps of a lane quarter meet
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 4);
+    uint64_t* oreport = xbar + 4;    // pair exit: the odd CTA's copy counts are ready (even CTA's)
+    uint64_t* pdone = oreport + 1;   // pair exit: the even CTA saw them all land (odd CTA's)
+    uint32_t* uses = reinterpret_cast<uint32_t*>(pdone + 1);  // [8] copies issued per stage
+    uint32_t* tmem_slot = uses + 8;
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(tmem_slot + 1);
     float* xch = reinterpret_cast<float*>(tmem_slot + 4);  // [2][EW][32] softmax partials
 
@@ -248,6 +282,9 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
         mbar_init(smem_u32(drain), 1);
         for (int i = 0; i < 2 * EW; ++i) mbar_init(smem_u32(&rbar[i]), 1);
         for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&xbar[i]), 64);
+        mbar_init(smem_u32(oreport), 1);
+        mbar_init(smem_u32(pdone), 1);
+        for (int i = 0; i < 8; ++i) uses[i] = 0u;
         *abort_flag = 0u;
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
@@ -271,7 +308,8 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
-            const bool stall = (args.flags & GEMM_FLAG_TEST_STALL) && blockIdx.x == 0;
+            const bool stall = ((args.flags & GEMM_FLAG_TEST_STALL) && blockIdx.x == 0) ||
+                               ((args.flags & GEMM_FLAG_TEST_STALL_PEER) && blockIdx.x == 1);
             int s = 0;
             uint32_t ph = 0;
             uint32_t armed = 0, armed_par = 0;  // per stage: armed and not yet seen consumed
@@ -332,6 +370,7 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                         }
                         armed |= 1u << s;
                         armed_par = (armed_par & ~(1u << s)) | (ph << s);
+                        if (PAIR) uses[s] += 1u;
                     }
                     if (++s == STAGES) {
                         s = 0;
@@ -339,21 +378,53 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                     }
                 }
             }
-            if (!ok) {
-                // Let our own copies land before the CTA's shared memory goes away.
-                if (PAIR && rank == 1) {
-                    // they count on the even CTA's barriers, which this CTA cannot
-                    // wait on: give them a fixed 200 us (a copy takes a few us)
-                    if (armed) {
+            if (PAIR) {
+                // Every copy of a pair counts on the even CTA's full[] barriers, so
+                // the even producer sees each copy either CTA issued land before the
+                // pair may leave (normal end or abort).  The odd producer reports its
+                // per-stage copy counts; a stage's copies all belong to its last
+                // phase (a producer issues use u + 1 of a stage only after use u was
+                // consumed), and the even producer makes that phase completable by
+                // counting the share that will never come -- the odd CTA's, by
+                // complete_tx, or its own, by arming the phase for the odd share
+                // alone -- then waits for it and acknowledges.  Both CTAs then stay
+                // resident until the exit cluster barrier.
+                const uint64_t lim = 3 * tmo + 1000000ull;
+                if (rank == 1) {
+                    mbar_arrive_cluster(mapa_shared(smem_u32(oreport), 0));
+                    if (!mbar_wait_peer(smem_u32(pdone), 0u, lim) && armed) {
+                        // no acknowledgement: give our copies a fixed 200 us
                         const uint64_t t0 = globaltimer_ns();
                         while (globaltimer_ns() - t0 < 200000ull) {
                         }
                     }
                 } else {
-                    for (int i = 0; i < STAGES; ++i)
-                        if (armed & (1u << i))
-                            tc_drain(smem_u32(&full[i]), (armed_par >> i) & 1u, tmo);
+                    const bool got = mbar_wait_peer(smem_u32(oreport), 0u, lim);
+                    for (int i = 0; i < STAGES; ++i) {
+                        if (!got) {  // no report: our own armed phases only
+                            if (!ok && (armed & (1u << i)))
+                                tc_drain(smem_u32(&full[i]), (armed_par >> i) & 1u, tmo);
+                            continue;
+                        }
+                        const uint32_t ne = uses[i];
+                        const uint32_t no = ld_peer_u32(mapa_shared(smem_u32(&uses[i]), 1));
+                        const uint32_t n = ne > no ? ne : no;
+                        if (n == 0) continue;
+                        if (ne == no + 1)
+                            mbar_complete_tx(smem_u32(&full[i]), L::STAGE_BYTES);
+                        else if (no == ne + 1)
+                            mbar_arrive_expect_tx(smem_u32(&full[i]), L::STAGE_BYTES);
+                        else if (ne != no)
+                            continue;
+                        tc_drain(smem_u32(&full[i]), (n - 1) & 1u, tmo);
+                    }
+                    if (got) mbar_arrive_cluster(mapa_shared(smem_u32(pdone), 1));
                 }
+            } else if (!ok) {
+                // Let our own copies land before the CTA's shared memory goes away.
+                for (int i = 0; i < STAGES; ++i)
+                    if (armed & (1u << i))
+                        tc_drain(smem_u32(&full[i]), (armed_par >> i) & 1u, tmo);
             }
         }
     } else if (warp == 1) {

@@ -80,6 +80,9 @@ typedef enum {
 #define GEMM_FLAG_TEST_STALL 0x80000000u /* test only: the first CTA's producer withholds one
                                             operand tile so its waits run out; with a short
                                             timeout_ms this exercises the timeout path */
+#define GEMM_FLAG_TEST_STALL_PEER 0x40000000u /* test only: as GEMM_FLAG_TEST_STALL, for the
+                                                 second CTA (tensor-core kernel: the odd CTA of
+                                                 the first CTA pair) */
 
 /*
  * Everything about a call besides (dtype, M, N, K, lda, ldb, ldc).  Pass NULL
