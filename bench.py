@@ -537,9 +537,12 @@ def run_ours(args):
             mx = statistics.median(tx)
             kx = px.info()["config"].kernel
             r = roofline_for(wx, kx, statistics.fmean(tx), pk, pk_kind, px.info()["num_sms"])
-            extra.append({"workload": name, "tflops": round(wx.flops / (mx * 1e-3) / 1e12, 2),
-                          "ms": round(mx, 4), "kernel": kx, "bn": px.info()["config"].bn,
-                          "bound": r["bound"], "frac": round(r["achieved"] / r["peak"], 4)})
+            entry = {"workload": name, "tflops": round(wx.flops / (mx * 1e-3) / 1e12, 2),
+                     "ms": round(mx, 4), "kernel": kx, "bn": px.info()["config"].bn,
+                     "bound": r["bound"], "frac": round(r["achieved"] / r["peak"], 4)}
+            if "frac_basis" in r:
+                entry["frac_basis"] = r["frac_basis"]
+            extra.append(entry)
             del dx, Cx, px
             torch.cuda.empty_cache()
         result["secondary"] = extra

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libgemm13.so")
 SOURCES = ["capi.cpp", "dispatch.cpp", "tc_sm103.cu", "sgemm_ffma.cu", "aux_kernels.cu",
-           "noalloc.cu"]
+           "skinny_tma.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-I", INCLUDE, "-I", CSRC]

@@ -148,6 +148,17 @@ int encode(CUtensorMap* m, int dtype, const void* base, int64_t cols, int64_t ro
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+}  // namespace
+
+int g13::tmap_encode_3d(CUtensorMap* m, int dtype, const void* base, int64_t cols, int64_t rows,
+                        int64_t ld, int64_t batches, int64_t bstride, uint32_t box_cols,
+                        uint32_t box_rows) {
+    return encode(m, dtype, base, cols, rows, ld, batches, bstride, box_cols, box_rows,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+namespace {
+
 bool cfg_is_split_skinny(const gemm_config_t& c) {
     return c.kernel == GEMM_KERNEL_SKINNY && c.split_k > 1;
 }
@@ -226,7 +237,19 @@ int make_plan(const Problem& p, const gemm_config_t* forced, gemm_plan_t* out_pl
         ws += static_cast<size_t>(round_up(
             p.epi.batch * tc_effective_splits(p.K, cfg.split_k) * p.M * p.N * 4, 256));
     }
-    if (cfg.kernel == GEMM_KERNEL_SKINNY && cfg.split_k > 1) {
+    if (cfg.kernel == GEMM_KERNEL_SKINNY && cfg.variant == SKINNY_VARIANT_TMA) {
+        // TMA skinny kernel: two partial-sum slots per SM for blocks cut between
+        // CTAs, then one arrival counter per (batch, block) -- at most batch x Q --
+        // zeroed here and reset by the kernel that consumes them
+        int64_t P, Q;
+        int dot;
+        skinny_geometry(p.M, p.N, p.epi.b_layout, &P, &Q, &dot);
+        pl->sk_off = ws;
+        ws += static_cast<size_t>(round_up(static_cast<int64_t>(skinny_tma_workspace_bytes(sms)), 256));
+        pl->sk_tags_off = ws;
+        pl->sk_ctr_bytes = static_cast<size_t>(round_up(p.epi.batch * Q * 4, 256));
+        ws += pl->sk_ctr_bytes;
+    } else if (cfg.kernel == GEMM_KERNEL_SKINNY && cfg.split_k > 1) {
         // split-K partial sums [batch][split_k][P][Q] FP32, then one arrival
         // counter per output group (at most batch x Q), zeroed here and reset
         // by the kernel that consumes them
@@ -364,9 +387,12 @@ int gemm_run(gemm_plan_t plan, const void* A, const void* B, void* C, const void
     lc.flags = ep.flags;
     lc.num_sms = plan->num_sms;
     lc.stream = st;
-    if (cfg_is_split_skinny(plan->cfg) || tc_splits_of(plan) > 1)
+    const bool skinny_ws = cfg_is_split_skinny(plan->cfg) ||
+                           (plan->cfg.kernel == GEMM_KERNEL_SKINNY &&
+                            plan->cfg.variant == SKINNY_VARIANT_TMA);
+    if (skinny_ws || tc_splits_of(plan) > 1)
         lc.sk_partials = reinterpret_cast<float*>(static_cast<char*>(plan->d_ws) + plan->sk_off);
-    if (cfg_is_split_skinny(plan->cfg))
+    if (skinny_ws)
         lc.sk_tags = reinterpret_cast<unsigned*>(static_cast<char*>(plan->d_ws) + plan->sk_tags_off);
     if (plan->sk_grid > 0) {
         lc.sk_partials = reinterpret_cast<float*>(static_cast<char*>(plan->d_ws) + plan->sk_off);
@@ -391,7 +417,19 @@ int gemm_run(gemm_plan_t plan, const void* A, const void* B, void* C, const void
         a.stride_b = ep.batch > 1 ? ep.stride_b : 0;
         a.dtype = p.dtype;
         a.b_layout = ep.b_layout;
-        ce = launch_skinny(cfg, a, s, e, lc);
+        // the TMA-streamed kernel when the large operand allows it on this run
+        if (cfg.variant == SKINNY_VARIANT_TMA && skinny_tma_aligned(a, s)) {
+            // the large operand's descriptor, re-encoded only when its pointer changes
+            const void* L = s.M <= s.N ? B : A;
+            std::lock_guard<std::mutex> lk(plan->mu);
+            if (plan->mapA_src != L) {
+                if (skinny_tma_encode(a, s, &plan->mapA) != GEMM_OK) return GEMM_ERR_CUDA;
+                plan->mapA_src = L;
+            }
+            ce = launch_skinny_tma(a, s, e, lc, cfg.num_ctas, plan->mapA);
+        } else {
+            ce = launch_skinny(cfg, a, s, e, lc);
+        }
         return map_cuda_error(ce);
     }
     if (ffma_small(cfg)) {

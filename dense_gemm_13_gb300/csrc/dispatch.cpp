@@ -128,6 +128,22 @@ int skinny_splits(const Problem& p, int num_sms) {
     return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(splits, 1024)));
 }
 
+// The TMA-streamed skinny kernel can run p: large operand rows (and batch
+// stride) 16-byte aligned for TMA, and the small operand (P <= 4 rows of K, as
+// FP32) fits shared memory beside the ring.
+bool skinny_tma_suits(const Problem& p) {
+    if (p.M == 0 || p.N == 0 || p.K == 0) return false;
+    int64_t P, Q;
+    int dot;
+    skinny_geometry(p.M, p.N, p.epi.b_layout, &P, &Q, &dot);
+    if (P > kSkinnyMax) return false;
+    const bool l_is_b = p.M <= p.N;
+    const int64_t ldl = l_is_b ? p.ldb : p.lda;
+    const int64_t sl = l_is_b ? p.epi.stride_b : p.epi.stride_a;
+    if (!stride_tma_ok(ldl, sl, p.epi.batch, dtype_size(p.dtype))) return false;
+    return skinny_tma_fits(P, p.K, p.dtype, dot);
+}
+
 // Split-K for the tensor-core kernel when its tiles cannot fill the GPU (small
 // M and N, long K): a rough time model -- waves of (tile, split) items, each
 // limited by its MMA work or by the HBM share its SM gets -- plus the partial
@@ -197,6 +213,19 @@ int choose_config(const Problem& p, int num_sms, gemm_config_t* out) {
         c.stages = 1;
         c.raster_group = 1;
         c.split_k = skinny_splits(p, num_sms);
+        // Dot mode (the large operand's rows hold K) streams through the TMA
+        // ring once the large operand has 2^20 elements or more: GB300, BF16,
+        // L2 flushed: 1 x 6144 x 6144 NK 31 vs 38 us, 6144 x 1 x 6144 31 vs 40,
+        // 6144 x 4 x 6144 (a strided small operand) 44 vs 300.  Axpy mode keeps the
+        // plain-load kernel, whose many CTAs spread over SMs of unequal memory
+        // bandwidth better than one CTA per SM does (1 x 6144 x 6144 KN 25 vs 33 us).
+        int64_t P, Q;
+        int dot;
+        skinny_geometry(M, N, p.epi.b_layout, &P, &Q, &dot);
+        if (dot && skinny_tma_suits(p) && bt * Q * K >= (int64_t(1) << 20)) {
+            c.variant = SKINNY_VARIANT_TMA;
+            c.split_k = 1;  // stream-K over the stages instead of fixed K slices
+        }
         *out = c;
         return GEMM_OK;
     }
@@ -313,6 +342,11 @@ int check_config(const Problem& p, const gemm_config_t& in, gemm_config_t* out) 
         case GEMM_KERNEL_SKINNY:
             c.stage_a = c.stage_b = 0;
             if (c.stream_k != 0) return GEMM_ERR_UNSUPPORTED;
+            if (c.variant != 0 && c.variant != SKINNY_VARIANT_TMA) return GEMM_ERR_UNSUPPORTED;
+            if (c.variant == SKINNY_VARIANT_TMA) {
+                if (!skinny_tma_suits(p)) return GEMM_ERR_UNSUPPORTED;
+                c.split_k = 1;  // the TMA kernel balances by stream-K, num_ctas caps its grid
+            }
             break;
         case GEMM_KERNEL_FFMA:
             if (p.dtype != GEMM_F32 || p.K == 0) return GEMM_ERR_UNSUPPORTED;

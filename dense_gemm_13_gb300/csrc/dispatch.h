@@ -26,6 +26,8 @@ bool stride_tma_ok(int64_t ld, int64_t bstride, int64_t batch, int esz);
 
 // K splits the skinny kernel uses for p (1 = none).
 int skinny_splits(const Problem& p, int num_sms);
+// Whether p can run the TMA-streamed skinny kernel.
+bool skinny_tma_suits(const Problem& p);
 // K splits for the tensor-core kernel with BN-wide tiles (1 = none).
 int tc_splits(const Problem& p, int num_sms, int bn);
 

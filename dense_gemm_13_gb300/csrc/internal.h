@@ -130,6 +130,34 @@ cudaError_t launch_skinny(const gemm_config_t& cfg, const SkinnyArgs& a, const S
 // large one; dot = 1 when the streamed operand has K contiguous.
 void skinny_geometry(int64_t M, int64_t N, int b_layout, int64_t* P, int64_t* Q, int* dot);
 
+// Skinny config variant that streams the large operand through shared memory
+// by TMA (csrc/skinny_tma.cu); the plain-load kernel is variant 0 and also
+// runs whenever the large operand's base address is not 16-byte aligned.
+constexpr int SKINNY_VARIANT_TMA = 1;
+// Host-side geometry of the TMA skinny kernel: K per pipeline stage and rows
+// (dot) or columns (axpy) per work block, for a dtype and mode.
+int64_t skinny_tma_stage_k(int dtype, int dot);
+int64_t skinny_tma_block(int dtype, int dot);
+// Whether P small-operand rows of length K fit the kernel's shared memory.
+bool skinny_tma_fits(int64_t P, int64_t K, int dtype, int dot);
+// Whether this run's large operand can be read by TMA (16-byte aligned base,
+// row stride and batch stride).
+bool skinny_tma_aligned(const SkinnyArgs& a, const Shape& s);
+// Stream-K over the large operand's stages: lc.sk_partials holds the partial
+// sums of blocks cut between CTAs (skinny_tma_workspace_bytes(lc.num_sms)),
+// lc.sk_tags one zeroed counter per (batch, block) (at most batch * Q).
+// num_ctas > 0 caps the grid (one CTA per SM otherwise).
+// tm: skinny_tma_encode's descriptor of this run's large operand.
+int skinny_tma_encode(const SkinnyArgs& a, const Shape& s, CUtensorMap* tm);
+cudaError_t launch_skinny_tma(const SkinnyArgs& a, const Shape& s, const EpiParams& e,
+                              const LaunchCtx& lc, int num_ctas, const CUtensorMap& tm);
+size_t skinny_tma_workspace_bytes(int num_sms);
+// 3-D tiled TMA descriptor without swizzle over [batches][rows][cols] (row
+// stride ld, batch stride bstride, in elements), box box_cols x box_rows.
+int tmap_encode_3d(CUtensorMap* m, int dtype, const void* base, int64_t cols, int64_t rows,
+                   int64_t ld, int64_t batches, int64_t bstride, uint32_t box_cols,
+                   uint32_t box_rows);
+
 // Copies [batch][rows][cols] (row stride ld, batch stride bstride, element
 // size esz) into a dense [batch][rows][dst_ld] buffer (dst and dst_ld * esz
 // multiples of 16 bytes, else cudaErrorInvalidValue).  Padding columns get

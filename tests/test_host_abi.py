@@ -140,6 +140,22 @@ def test_dispatch_buckets(lib):
     assert sel("bf16", 4096, 4096, 4096, flags=g13.FLAG_FP32_TENSOR).kernel == "tc"
 
 
+def test_dispatch_skinny_tma(lib):
+    # large dot-mode problems (the large operand's rows hold K) with 16-byte-aligned
+    # rows stream through the TMA ring (variant 1); axpy mode (B in KN layout with M
+    # small), small problems and unaligned rows take the plain-load kernel (variant 0)
+    for M, N, K, lay in ((1, 6144, 6144, "nk"), (6144, 1, 6144, "kn"), (6144, 4, 6144, "kn"),
+                         (2, 6144, 4096, "nk"), (1000, 1, 6144, "nk")):
+        c = sel("bf16", M, N, K, lay)
+        assert (c.kernel, c.variant, c.split_k) == ("skinny", 1, 1), (M, N, K, lay)
+    for M, N, K, lay in ((1, 6144, 6144, "kn"), (4, 6144, 6144, "kn"), (1, 1000, 1000, "nk"),
+                         (6144, 1, 4097, "kn"), (1, 6144, 4097, "nk")):
+        assert sel("bf16", M, N, K, lay).variant == 0, (M, N, K, lay)
+    # P = 4 rows of K as FP32 beside a 4-stage ring: K = 6144 fits, 16384 does not
+    assert sel("bf16", 6144, 4, 6144).variant == 1
+    assert sel("bf16", 6144, 4, 16384).variant == 0
+
+
 def test_dispatch_small_fp32(lib):
     # 32 x 32 tiles from plain loads when the 128 x 128 tiles number at most one per
     # eight SMs and K <= 512; otherwise the TMA-fed kernel (stream-K or whole tiles)
