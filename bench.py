@@ -93,15 +93,15 @@ def peaks():
             "sm_max_mhz": 2070.0}, "fallback"
 
 
-KERNEL_SOURCES = {"tc": "tc_sm103.cu", "ffma": "sgemm_ffma.cu", "skinny": "aux_kernels.cu",
-                  "tf32x3": "tc_sm103.cu"}
+KERNEL_SOURCES = {"tc": ("tc_sm103.cu",), "ffma": ("sgemm_ffma.cu",),
+                  "skinny": ("aux_kernels.cu", "skinny_tma.cu"), "tf32x3": ("tc_sm103.cu",)}
 
 
 def source_hash(kernel: str) -> str:
-    """Hash of the files that make up one kernel family (its .cu and the shared headers)."""
+    """Hash of the files that make up one kernel family (its .cu files and the shared headers)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_gemm_13_gb300", "csrc")
-    for f in (KERNEL_SOURCES[kernel], "epilogue.cuh", "ptx.cuh", "internal.h"):
+    for f in (*KERNEL_SOURCES[kernel], "epilogue.cuh", "ptx.cuh", "internal.h"):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
