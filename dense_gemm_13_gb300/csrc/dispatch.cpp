@@ -322,6 +322,13 @@ int choose_config(const Problem& p, int num_sms, gemm_config_t* out) {
                 c.stages = 6;
                 c.variant = TC_VARIANT_PAIR;
                 c.raster_group = static_cast<int32_t>(std::min<int64_t>(16, cdiv(M, 256)));
+                // C rows TMA cannot store (e.g. N odd): the per-row epilogue of a pair
+                // tile outlasts its main loop with four epilogue warps, so use eight
+                const int osz = dtype_size(p.epi.out_dtype);
+                if ((p.ldc * osz) % 16 != 0 || (bt > 1 && (p.epi.stride_c * osz) % 16 != 0)) {
+                    c.variant = TC_VARIANT_PAIR8;
+                    c.stages = 5;
+                }
             }
         }
     }
@@ -390,7 +397,8 @@ int check_config(const Problem& p, const gemm_config_t& in, gemm_config_t* out) 
                   (c.variant == 1 && ((c.bn == 256 && c.stages == 3) ||
                                       (c.bn == 128 && c.stages == 4) ||
                                       (c.bn == 512 && c.stages == 1))) ||
-                  (c.variant == TC_VARIANT_PAIR && c.bn == 256 && (c.stages == 6 || c.stages == 4))))
+                  (c.variant == TC_VARIANT_PAIR && c.bn == 256 && (c.stages == 6 || c.stages == 4)) ||
+                  (c.variant == TC_VARIANT_PAIR8 && c.bn == 256 && c.stages == 5)))
                 return GEMM_ERR_UNSUPPORTED;
 
             if (tc_is_pair(c) && c.split_k > 1) return GEMM_ERR_UNSUPPORTED;

@@ -83,7 +83,12 @@ cudaError_t launch_tf32_split(const float* X, int64_t rows, int64_t cols, int64_
                               int64_t ldo, cudaStream_t stream);
 // TC config variant that runs CTA pairs (tcgen05 cta_group::2, 256-row tiles).
 constexpr int TC_VARIANT_PAIR = 2;
-inline bool tc_is_pair(const gemm_config_t& cfg) { return cfg.variant == TC_VARIANT_PAIR; }
+// CTA pairs with eight epilogue warps (two per TMEM lane quarter) and 5 stages:
+// for C layouts TMA cannot store, whose per-row epilogue outlasts the main loop.
+constexpr int TC_VARIANT_PAIR8 = 3;
+inline bool tc_is_pair(const gemm_config_t& cfg) {
+    return cfg.variant == TC_VARIANT_PAIR || cfg.variant == TC_VARIANT_PAIR8;
+}
 // Rows of a K-major B box: the tile's columns, split between the CTAs of a
 // pair, at most 256 (a TMA box dimension's limit; 512-wide tiles take two).
 inline int tc_b_box_rows(const gemm_config_t& cfg) {

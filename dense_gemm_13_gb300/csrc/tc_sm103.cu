@@ -175,9 +175,10 @@ __host__ __device__ constexpr int tc_smem_total() {
     // ring + epilogue tiles + full/empty per stage + tfull/tempty x2 + drain
     // + residual barriers (2 per epilogue warp) + softmax exchange barriers (4)
     // + pair exit barriers (2) + per-stage copy counts (8) + tmem slot + abort
-    // flag + softmax exchange values [2][EW][32] floats
+    // flag + softmax exchange values [2][EW][32] floats (single CTAs only: the
+    // row softmax never runs on CTA pairs)
     return 1024 + tc_bar_off<BN, STAGES, EW, PAIR, K3>() + (2 * STAGES + 11 + 2 * EW) * 8 + 32 +
-           16 + 2 * EW * 32 * 4;
+           16 + (PAIR ? 0 : 2 * EW * 32 * 4);
 }
 
 // 32-bit arithmetic: the host keeps the tile count below 2^31.
@@ -1157,7 +1158,8 @@ cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& 
     X(128, 4, 8, 1, false)   \
     X(512, 1, 8, 1, false)   \
     X(256, 6, 4, 2, true)    \
-    X(256, 4, 4, 2, true)
+    X(256, 4, 4, 2, true)    \
+    X(256, 5, 8, 3, true)
 
 template <bool B_KN>
 cudaError_t launch_tc_layout(const gemm_config_t& cfg, int dtype, const CUtensorMap& tmA,

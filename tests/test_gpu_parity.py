@@ -66,7 +66,9 @@ TC_CONFIGS = [g13.Config("tc", 128, 256, 64, 4), g13.Config("tc", 128, 256, 64, 
               g13.Config("tc", 128, 128, 64, 4, variant=1),
               # CTA pairs (tcgen05 cta_group::2) on 256 x 256 tiles
               g13.Config("tc", 128, 256, 64, 6, variant=2),
-              g13.Config("tc", 128, 256, 64, 4, variant=2)]
+              g13.Config("tc", 128, 256, 64, 4, variant=2),
+              # CTA pairs with eight epilogue warps (C rows TMA cannot store)
+              g13.Config("tc", 128, 256, 64, 5, variant=3)]
 
 
 @pytest.mark.parametrize("cfg", TC_CONFIGS, ids=lambda c: f"bn{c.bn}s{c.stages}v{c.variant}")
@@ -97,6 +99,8 @@ def test_tc_pair_epilogue_batched():
                      out_dtype="bf16")
         full_check(Run(w, config=g13.Config("tc", 128, 256, 64, 6, variant=2)))
         full_check(Run(w, config=g13.Config("tc", 128, 256, 64, 4, variant=2), ldc_pad=1))
+        full_check(Run(w, config=g13.Config("tc", 128, 256, 64, 5, variant=3), ldc_pad=1))
+        full_check(Run(w, config=g13.Config("tc", 128, 256, 64, 5, variant=3)))
 
 
 RES_CONFIGS = [g13.Config("tc", 128, 256, 64, 3, variant=1, num_ctas=3),

@@ -125,7 +125,10 @@ def test_dispatch_buckets(lib):
     c = sel("bf16", 256, 256, 4096, "nk")
     assert (c.kernel, c.variant) == ("tc", 0) and c.split_k > 1   # split-K runs single CTAs
     c = sel("bf16", 8192, 8192, 8192, "nk", sms=1)
-    assert c.variant != 2                                    # a pair needs two SMs
+    assert c.variant not in (2, 3)                           # a pair needs two SMs
+    c = sel("bf16", 3001, 3001, 3001)                        # C rows of 12004 bytes: no TMA store
+    assert (c.kernel, c.variant, c.stages) == ("tc", 3, 5)   # pairs with eight epilogue warps
+    assert sel("bf16", 3001, 3000, 3001).variant == 2        # 12000-byte rows: TMA stores
     for M, N in ((1, 6144), (6144, 1), (0, 10), (10, 0)):
         assert sel("bf16", M, N, 1000).kernel == "skinny", (M, N)
     assert sel("bf16", 512, 512, 0).kernel == "skinny"      # K = 0: epilogue only
