@@ -18,7 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libgemm13.so")
-SOURCES = ["capi.cpp", "dispatch.cpp", "tc_sm103.cu", "sgemm_ffma.cu", "aux_kernels.cu",
+SOURCES = ["capi.cpp", "dispatch.cpp", "tc_sm103.cu", "tc_any_kn.cu", "tc_any_nk.cu", "tc_spec_kn.cu",
+           "tc_spec_nk.cu", "tc_sk_kn.cu", "tc_sk_nk.cu", "sgemm_ffma.cu", "aux_kernels.cu",
            "skinny_tma.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

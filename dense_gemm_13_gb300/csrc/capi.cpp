@@ -69,6 +69,7 @@ struct gemm_plan_s {
     int64_t stride_as = 0, stride_bs = 0;
     size_t sk_off = 0, sk_tags_off = 0;   // stream-K / split-K partial slots and tags in d_ws
     size_t sk_ctr_bytes = 0;              // skinny split-K arrival counters
+    size_t sk_tag_bytes = 0;              // stream-K tags (zeroed once)
     int64_t sk_grid = 0;
     size_t t3_a_off = 0, t3_b_off = 0;    // 3xTF32 split buffers [batch][hi, lo][rows][t3_ld]
     int64_t t3_ld = 0;
@@ -262,6 +263,18 @@ int make_plan(const Problem& p, const gemm_config_t* forced, gemm_plan_t* out_pl
         pl->sk_ctr_bytes = static_cast<size_t>(round_up(p.epi.batch * Q * 4, 256));
         ws += pl->sk_ctr_bytes;
     }
+    if (cfg.kernel == GEMM_KERNEL_TC && cfg.stream_k) {
+        // Stream-K on the tensor cores: one 128-row x BN partial-sum slot and
+        // eight tags (one per epilogue warp) per CTA of the persistent grid.
+        int64_t grid = sms;
+        if (cfg.num_ctas > 0 && cfg.num_ctas < grid) grid = cfg.num_ctas;
+        pl->sk_grid = grid;
+        pl->sk_off = ws;
+        ws += static_cast<size_t>(grid) * 128 * static_cast<size_t>(cfg.bn) * 4;
+        pl->sk_tags_off = ws;
+        pl->sk_tag_bytes = static_cast<size_t>(grid) * 8 * 4;
+        ws += static_cast<size_t>(round_up(grid * 8 * 4, 256));
+    }
     if (cfg.kernel == GEMM_KERNEL_FFMA && cfg.stream_k) {
         // Persistent grid: every CTA the device can hold at once (the launch is
         // cooperative), and one 64 KB partial-sum slot plus a tag per CTA.
@@ -276,14 +289,14 @@ int make_plan(const Problem& p, const gemm_config_t* forced, gemm_plan_t* out_pl
         pl->sk_off = ws;
         ws += static_cast<size_t>(grid) * ffma_partial_slot_bytes(cfg);
         pl->sk_tags_off = ws;
+        pl->sk_tag_bytes = static_cast<size_t>(grid) * 4;
         ws += static_cast<size_t>(round_up(grid * 4, 256));
     }
     ce = cudaMalloc(reinterpret_cast<void**>(&pl->d_status), sizeof(unsigned));
     if (ce == cudaSuccess) ce = cudaMemset(pl->d_status, 0, sizeof(unsigned));
     if (ce == cudaSuccess && ws > 0) ce = cudaMalloc(&pl->d_ws, ws);
-    if (ce == cudaSuccess && pl->sk_grid > 0)
-        ce = cudaMemset(static_cast<char*>(pl->d_ws) + pl->sk_tags_off, 0,
-                        static_cast<size_t>(pl->sk_grid) * 4);
+    if (ce == cudaSuccess && pl->sk_tag_bytes > 0)
+        ce = cudaMemset(static_cast<char*>(pl->d_ws) + pl->sk_tags_off, 0, pl->sk_tag_bytes);
     if (ce == cudaSuccess && pl->sk_ctr_bytes > 0)
         ce = cudaMemset(static_cast<char*>(pl->d_ws) + pl->sk_tags_off, 0, pl->sk_ctr_bytes);
     if (ce != cudaSuccess) {

@@ -388,7 +388,10 @@ int check_config(const Problem& p, const gemm_config_t& in, gemm_config_t* out) 
             return GEMM_OK;
         case GEMM_KERNEL_TC:
             if (p.dtype == GEMM_F32 || p.K == 0) return GEMM_ERR_UNSUPPORTED;
-            if (c.stream_k != 0) return GEMM_ERR_UNSUPPORTED;
+            // stream-K: whole-tile epilogues only (no split-K, no row softmax)
+            if (c.stream_k < 0 || c.stream_k > 1) return GEMM_ERR_UNSUPPORTED;
+            if (c.stream_k && (c.split_k > 1 || p.epi.act == GEMM_ACT_SOFTMAX || !tc_has_spec(c)))
+                return GEMM_ERR_UNSUPPORTED;
             if (c.bm != 128 || c.bk != 64) return GEMM_ERR_UNSUPPORTED;
             // (BN, stages) pairs with 4 epilogue warps (variant 0) or 8 (variant 1);
             // variant 2: CTA pairs on 256 x 256 tiles, no split-K

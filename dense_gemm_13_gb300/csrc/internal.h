@@ -86,6 +86,41 @@ constexpr int TC_VARIANT_PAIR = 2;
 // CTA pairs with eight epilogue warps (two per TMEM lane quarter) and 5 stages:
 // for C layouts TMA cannot store, whose per-row epilogue outlasts the main loop.
 constexpr int TC_VARIANT_PAIR8 = 3;
+// Tensor-core kernels by epilogue kind.  TC_EK_ANY runs every epilogue (the
+// row softmax; C rows TMA cannot store); the others store C by TMA and hold
+// only one kind of epilogue: scale only, bias / ReLU / residual, or GELU (with
+// or without bias, no residual).  A kernel whose loop holds only the steps its
+// tiles run fetches far fewer instructions per tile.
+constexpr int TC_EK_ANY = 0, TC_EK_PLAIN = 1, TC_EK_BIAS = 2, TC_EK_GELU = 3;
+// The launchers of each part (tc_any_*.cu, tc_spec_*.cu, tc_sk_*.cu); the spec
+// ones take the kind, and the spec and stream-K ones the configurations of
+// tc_has_spec only.
+cudaError_t launch_tc_any_kn(const gemm_config_t& cfg, int dtype, const CUtensorMap& tmA,
+                             const CUtensorMap& tmB, const TcEpiMaps* em, const Shape& s,
+                             const EpiParams& e, const LaunchCtx& lc, const EpiParams* fe);
+cudaError_t launch_tc_any_nk(const gemm_config_t& cfg, int dtype, const CUtensorMap& tmA,
+                             const CUtensorMap& tmB, const TcEpiMaps* em, const Shape& s,
+                             const EpiParams& e, const LaunchCtx& lc, const EpiParams* fe);
+cudaError_t launch_tc_spec_kn(int ek, const gemm_config_t& cfg, int dtype, const CUtensorMap& tmA,
+                              const CUtensorMap& tmB, const TcEpiMaps* em, const Shape& s,
+                              const EpiParams& e, const LaunchCtx& lc, const EpiParams* fe);
+cudaError_t launch_tc_spec_nk(int ek, const gemm_config_t& cfg, int dtype, const CUtensorMap& tmA,
+                              const CUtensorMap& tmB, const TcEpiMaps* em, const Shape& s,
+                              const EpiParams& e, const LaunchCtx& lc, const EpiParams* fe);
+cudaError_t launch_tc_sk_kn(const gemm_config_t& cfg, int dtype, const CUtensorMap& tmA,
+                            const CUtensorMap& tmB, const TcEpiMaps* em, const Shape& s,
+                            const EpiParams& e, const LaunchCtx& lc, const EpiParams* fe);
+cudaError_t launch_tc_sk_nk(const gemm_config_t& cfg, int dtype, const CUtensorMap& tmA,
+                            const CUtensorMap& tmB, const TcEpiMaps* em, const Shape& s,
+                            const EpiParams& e, const LaunchCtx& lc, const EpiParams* fe);
+// Whether cfg has kernels specialised by epilogue kind and stream-K kernels.
+bool tc_has_spec(const gemm_config_t& cfg);
+cudaError_t tc_preload_sk_kn();
+cudaError_t tc_preload_sk_nk();
+cudaError_t tc_preload_any_kn();
+cudaError_t tc_preload_any_nk();
+cudaError_t tc_preload_spec_kn();
+cudaError_t tc_preload_spec_nk();
 inline bool tc_is_pair(const gemm_config_t& cfg) {
     return cfg.variant == TC_VARIANT_PAIR || cfg.variant == TC_VARIANT_PAIR8;
 }

@@ -111,6 +111,25 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, bool p
                  "l"(reinterpret_cast<uint64_t>(src)), "r"(pred ? 4 : 0)
                  : "memory");
 }
+// 16-byte asynchronous copy from global to shared memory of the first `bytes`
+// (0..16) bytes at src; the rest of the 16 destination bytes are zero-filled.
+// Both addresses 16-byte aligned; with bytes == 0 nothing is read (src must
+// still be a valid address).
+__device__ __forceinline__ void cp_async_16z(uint32_t dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 16, %2;" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+                 : "memory");
+}
+// Release store / acquire load of a flag in global memory, at GPU scope.
+__device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // Waits for all of this thread's cp.async copies.
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
@@ -341,6 +360,22 @@ __device__ __forceinline__ void tmem_st_wait() {
 
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// tcgen05.wait::ld that names the registers of the load it waits for, so that
+// no use of them can be scheduled above the wait (the load fills them
+// asynchronously; used when a next load is issued before the current values
+// are consumed).
+__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                   "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                   "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
 }
 
 }  // namespace g13

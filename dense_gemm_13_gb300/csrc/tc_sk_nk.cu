@@ -1,0 +1,29 @@
+// tc_sk_nk.cu -- the stream-K tensor-core kernels (any epilogue), K-major ([N, K]) B.
+#include "tc_kernel.cuh"
+
+namespace g13 {
+
+cudaError_t launch_tc_sk_nk(const gemm_config_t& cfg, int dtype, const CUtensorMap& tmA,
+                            const CUtensorMap& tmB, const TcEpiMaps* em, const Shape& s,
+                            const EpiParams& e, const LaunchCtx& lc, const EpiParams* fe) {
+#define G13_TC_LAUNCH(BN, ST, EW, VAR, PAIR)                                                      \
+    if (cfg.bn == BN && cfg.stages == ST && cfg.variant == VAR)                                   \
+        return launch_tc_t<BN, ST, false, EW, PAIR, false, TC_EK_ANY, true>(cfg, dtype, tmA, tmB, em, s, \
+                                                                         e, lc, fe);
+    G13_TC_SPEC_CONFIGS(G13_TC_LAUNCH)
+#undef G13_TC_LAUNCH
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t tc_preload_sk_nk() {
+    cudaFuncAttributes fa;
+    cudaError_t err = cudaSuccess;
+#define G13_TC_PRELOAD(BN, ST, EW, VAR, PAIR)                                                     \
+    if (err == cudaSuccess)                                                                       \
+        err = cudaFuncGetAttributes(&fa, tc_gemm_kernel<BN, ST, false, EW, PAIR, false, TC_EK_ANY, true>);
+    G13_TC_SPEC_CONFIGS(G13_TC_PRELOAD)
+#undef G13_TC_PRELOAD
+    return err;
+}
+
+}  // namespace g13

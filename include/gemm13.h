@@ -136,11 +136,15 @@ typedef struct {
                              plain loads for small M x N (bm = bn = bk = 32, any stride or
                              alignment, no stream-K); TC: 0 single CTAs with
                              4 epilogue warps, 1 single CTAs with 8 epilogue warps (short K),
-                             2 CTA pairs (cta_group::2, 256 x 256 tiles, no split-K);
+                             2 CTA pairs (cta_group::2, 256 x 256 tiles, no split-K),
+                             3 CTA pairs with 8 epilogue warps (bn 256, 5 stages);
                              TF32X3: 0 single CTAs (bn 128), 2 CTA pairs (bn 256) */
-    int32_t stream_k;     /* FFMA: 1 = persistent grid with (tile, K-step) units split evenly
-                             over the CTAs; tiles cut between CTAs are summed in a fixed order
-                             (deterministic).  Needs a plan workspace of grid x 64 KB. */
+    int32_t stream_k;     /* FFMA and TC: 1 = persistent grid with (tile, K-step) units split
+                             evenly over the CTAs (CTA pairs); a tile cut between them is
+                             finished by the holder of its first K step, which adds the others'
+                             partial sums in a fixed order (deterministic).  Needs a plan
+                             workspace of grid x 64 KB (FFMA) or grid x 128 x bn x 4 bytes (TC);
+                             TC: no split-K, no row softmax. */
 } gemm_config_t;
 
 typedef struct gemm_plan_s* gemm_plan_t;

@@ -120,6 +120,49 @@ def test_tc_residual_across_tiles(cfg, K):
     full_check(Run(w, config=cfg))
 
 
+SK_CONFIGS = [g13.Config("tc", 128, 256, 64, 4, stream_k=1), g13.Config("tc", 128, 128, 64, 6, stream_k=1),
+              g13.Config("tc", 128, 256, 64, 3, variant=1, stream_k=1),
+              g13.Config("tc", 128, 256, 64, 6, variant=2, stream_k=1),
+              g13.Config("tc", 128, 256, 64, 5, variant=3, stream_k=1)]
+
+
+@pytest.mark.parametrize("num_ctas", [0, 2, 6, 14])
+@pytest.mark.parametrize("cfg", SK_CONFIGS, ids=lambda c: f"bn{c.bn}s{c.stages}v{c.variant}")
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+def test_tc_stream_k_exact(cfg, layout, num_ctas):
+    # Tensor-core stream-K: 3 x 3 (pairs: 2 x 3) tiles x 16 K blocks, ragged edges,
+    # split over 1, 3 or 7 CTAs (pairs) or the whole GPU, where a tile is cut
+    # between up to 16 holders.  Integer inputs: exact in any summation order.
+    w = _int_workload("bf16", layout, 300, 600, 1000)
+    c = g13.Config(cfg.kernel, cfg.bm, cfg.bn, cfg.bk, cfg.stages, variant=cfg.variant,
+                   stream_k=1, num_ctas=num_ctas)
+    run = Run(w, config=c)
+    assert run.info["config"].stream_k == 1 and run.info["workspace_bytes"] > 0
+    C = run.run().result()
+    _, cref, _ = run.oracle()
+    assert np.array_equal(C, cref.reshape(C.shape)), f"{c}"
+    assert run.guard_ok()
+    C2 = run.run().result()  # bit-identical again (fixed order of the partial sums)
+    assert np.array_equal(C, C2)
+    assert g13.gemm_plan_status(run.plan) == 0
+
+
+@pytest.mark.parametrize("cfg", SK_CONFIGS, ids=lambda c: f"bn{c.bn}s{c.stages}v{c.variant}")
+def test_tc_stream_k_epilogue_batched(cfg):
+    # every epilogue step on a finisher's sum of partials, BF16 out through TMA
+    # stores (and, with an odd ldc, the per-row store path), two batches
+    w = Workload("tc_sk_epi", "bf16", 700, 520, 1500, batch=2, b_layout="nk", bias=True,
+                 act="gelu", residual=True, beta=0.5, alpha=0.25, out_dtype="bf16")
+    c = g13.Config(cfg.kernel, cfg.bm, cfg.bn, cfg.bk, cfg.stages, variant=cfg.variant,
+                   stream_k=1, num_ctas=10)
+    full_check(Run(w, config=c))
+    full_check(Run(w, config=c, ldc_pad=1))
+    # FP32 out with the residual read by TMA
+    w2 = Workload("tc_sk_res", "f16", 520, 700, 1300, b_layout="kn", bias=True, act="relu",
+                  residual=True, alpha=0.5, beta=0.75)
+    full_check(Run(w2, config=c))
+
+
 # ---------------------------------------------------------------- 3xTF32 (FP32 on tensor cores)
 TF32X3_CONFIGS = [g13.Config("tf32x3", 128, 256, 32, 3, variant=2),
                   g13.Config("tf32x3", 128, 128, 32, 3)]

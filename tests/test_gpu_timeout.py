@@ -73,3 +73,30 @@ def test_pair_withheld_tile_times_out_and_context_survives(who, layout):
     C2 = run.run().result()
     run.check(C2)
     assert g13.gemm_plan_status(run.plan) == 0
+
+
+@pytest.mark.parametrize("layout", ["nk", "kn"])
+def test_stream_k_missing_partial_times_out_and_context_survives(layout):
+    # Stream-K over 3 CTAs: 8 tiles of 32 K blocks, two waves of whole tiles, then
+    # the last two tiles' 64 units split 21 / 21 / 22, so the second CTA's range
+    # starts inside the seventh tile, whose finisher (the first CTA) waits for
+    # that CTA's partial sums.  With GEMM_FLAG_TEST_STALL_PEER the second CTA
+    # withholds its first box: its own waits run out, and so does the first
+    # CTA's wait for its tags; both exit and the status reads
+    # GEMM_ERR_DEVICE_TIMEOUT.
+    cfg = g13.Config("tc", 128, 256, 64, 4, stream_k=1, num_ctas=3)
+    w = Workload(f"stall_sk_{layout}", "bf16", 512, 512, 2048, b_layout=layout)
+    t = w.make(7)
+    ldb = w.N if layout == "kn" else w.K
+    stalled = g13.gemm_plan("bf16", w.M, w.N, w.K, w.K, ldb, w.N,
+                            g13.Epilogue(b_layout=layout, flags=g13.FLAG_TEST_STALL_PEER,
+                                         timeout_ms=100), cfg)
+    assert stalled.info()["config"].stream_k == 1
+    A, B = t["A"].cuda(), t["B"].cuda()
+    C = torch.zeros((w.M, w.N), dtype=torch.float32, device="cuda")
+    g13.gemm_run(stalled, A, B, C)
+    assert g13.gemm_plan_status(stalled) == -5
+    run = Run(w, tensors=t, config=cfg)
+    C2 = run.run().result()
+    run.check(C2)
+    assert g13.gemm_plan_status(run.plan) == 0
