@@ -93,8 +93,11 @@ def peaks():
             "sm_max_mhz": 2070.0}, "fallback"
 
 
-KERNEL_SOURCES = {"tc": ("tc_sm103.cu",), "ffma": ("sgemm_ffma.cu",),
-                  "skinny": ("aux_kernels.cu", "skinny_tma.cu"), "tf32x3": ("tc_sm103.cu",)}
+KERNEL_SOURCES = {"tc": ("tc_kernel.cuh", "tc_sm103.cu", "tc_any_kn.cu", "tc_any_nk.cu",
+                         "tc_spec_kn.cu", "tc_spec_nk.cu", "tc_sk_kn.cu", "tc_sk_nk.cu"),
+                  "ffma": ("sgemm_ffma.cu",),
+                  "skinny": ("aux_kernels.cu", "skinny_tma.cu"),
+                  "tf32x3": ("tc_kernel.cuh", "tc_any_nk.cu")}
 
 
 def source_hash(kernel: str) -> str:
