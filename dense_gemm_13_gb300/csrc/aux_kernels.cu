@@ -115,33 +115,41 @@ __device__ __forceinline__ float ldf(const T* p) {
     return to_f<T>(__ldg(p));
 }
 
-// VW elements at an unaligned (or short) position p: the 16-byte-aligned
-// chunk holding the first element and, only when the wanted bytes reach into
-// it, the next one; then a shift by the misalignment (the same for every lane
-// of a warp here, so the switch does not diverge).  Both chunks hold at least
-// one wanted element, so nothing outside the operand's pages is touched.
+// VW elements at an unaligned (or short) position p, in two steps so that the
+// loads of several positions are in flight before any is used: load_pair
+// fetches the 16-byte-aligned chunk holding the first element and, only when
+// the wanted bytes reach into it, the next one (both hold at least one wanted
+// element, so nothing outside the operand's pages is touched); pair_shift then
+// shifts by the misalignment with selects and funnel shifts (no branches) and
+// zero-fills past n_valid.
+struct RawPair {
+    uint4 lo, hi;
+};
 template <typename T, int VW>
-__device__ __forceinline__ uint4 load_raw_unaligned(const T* p, int n_valid) {
+__device__ __forceinline__ RawPair load_pair(const T* p, int n_valid) {
     const uintptr_t a = reinterpret_cast<uintptr_t>(p);
     const uint4* base = reinterpret_cast<const uint4*>(a & ~static_cast<uintptr_t>(15));
     const int sh = static_cast<int>(a & 15);  // bytes, a multiple of sizeof(T)
-    const uint4 lo = __ldg(base);
-    const uint4 hi = sh + n_valid * static_cast<int>(sizeof(T)) > 16 ? __ldg(base + 1)
-                                                                     : make_uint4(0, 0, 0, 0);
-    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-    uint32_t o[4];
+    RawPair r;
+    r.lo = n_valid > 0 ? __ldg(base) : make_uint4(0, 0, 0, 0);
+    r.hi = n_valid > 0 && sh + n_valid * static_cast<int>(sizeof(T)) > 16 ? __ldg(base + 1)
+                                                                          : make_uint4(0, 0, 0, 0);
+    return r;
+}
+template <typename T, int VW>
+__device__ __forceinline__ uint4 pair_shift(const RawPair& c, const T* p, int n_valid) {
+    const int sh = static_cast<int>(reinterpret_cast<uintptr_t>(p) & 15);
     const int wo = sh >> 2;
+    const uint32_t w[8] = {c.lo.x, c.lo.y, c.lo.z, c.lo.w, c.hi.x, c.hi.y, c.hi.z, c.hi.w};
+    uint32_t sw[5];  // words wo .. wo + 4
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        uint32_t x0, x1;
-        switch (wo) {  // o[j] from words wo + j, wo + j + 1 (static indices only)
-            case 0: x0 = w[j]; x1 = w[j + 1]; break;
-            case 1: x0 = w[j + 1]; x1 = w[j + 2]; break;
-            case 2: x0 = w[j + 2]; x1 = w[j + 3]; break;
-            default: x0 = w[j + 3]; x1 = j + 4 < 8 ? w[j + 4] : 0u; break;
-        }
-        o[j] = (sh & 2) ? __funnelshift_r(x0, x1, 16) : x0;
+    for (int j = 0; j < 5; ++j) {
+        const uint32_t a0 = w[j], a1 = w[j + 1], a2 = w[j + 2], a3 = j + 3 < 8 ? w[j + 3] : 0u;
+        sw[j] = wo == 0 ? a0 : wo == 1 ? a1 : wo == 2 ? a2 : a3;
     }
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o[j] = (sh & 2) ? __funnelshift_r(sw[j], sw[j + 1], 16) : sw[j];
     uint4 r = make_uint4(o[0], o[1], o[2], o[3]);
     if (n_valid < VW) {  // elements past n_valid read as zero
         T* e = reinterpret_cast<T*>(&r);
@@ -150,6 +158,11 @@ __device__ __forceinline__ uint4 load_raw_unaligned(const T* p, int n_valid) {
             if (i >= n_valid) e[i] = T(0.0f);
     }
     return r;
+}
+template <typename T, int VW>
+__device__ __forceinline__ uint4 load_raw_unaligned(const T* p, int n_valid) {
+    if (n_valid <= 0) return make_uint4(0, 0, 0, 0);
+    return pair_shift<T, VW>(load_pair<T, VW>(p, n_valid), p, n_valid);
 }
 
 // 16 raw bytes (VW elements of T): one 16-byte load when `vec` (aligned, all in
@@ -253,7 +266,7 @@ __device__ __forceinline__ void skinny_out(const SkinnyParams& sp, int64_t b, in
 // 16-byte aligned (a separate instantiation, so the aligned one keeps its
 // registers).
 template <typename T, int PMAX, bool UA>
-__global__ void __launch_bounds__(256, PMAX == 1 ? 3 : 2) skinny_dot_kernel(const SkinnyParams sp) {
+__global__ void __launch_bounds__(256, PMAX == 1 && !UA ? 3 : 2) skinny_dot_kernel(const SkinnyParams sp) {
     constexpr int VW = 16 / sizeof(T);
     const int lane = threadIdx.x & 31;
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
@@ -277,11 +290,28 @@ __global__ void __launch_bounds__(256, PMAX == 1 ? 3 : 2) skinny_dot_kernel(cons
             for (int i = 0; i < PMAX; ++i) acc[i] = 0.0f;
             for (int64_t kb = k0 + lane * VW; kb < k1; kb += 32 * VW * U) {
                 uint4 raw[U];
+                if constexpr (UA) {
+                    // every chunk load of the U positions first, then the shifts
+                    RawPair pr[U];
 #pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int64_t k = kb + u * 32 * VW;
-                    const int nv = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(VW), k1 - k)));
-                    raw[u] = load_raw<T, VW, UA>(lrow + k, sp.l_vec && nv == VW, nv);
+                    for (int u = 0; u < U; ++u) {
+                        const int64_t k = kb + u * 32 * VW;
+                        const int nv = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(VW), k1 - k)));
+                        pr[u] = load_pair<T, VW>(lrow + k, nv);
+                    }
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int64_t k = kb + u * 32 * VW;
+                        const int nv = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(VW), k1 - k)));
+                        raw[u] = pair_shift<T, VW>(pr[u], lrow + k, nv);
+                    }
+                } else {
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int64_t k = kb + u * 32 * VW;
+                        const int nv = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(VW), k1 - k)));
+                        raw[u] = load_raw<T, VW, UA>(lrow + k, sp.l_vec && nv == VW, nv);
+                    }
                 }
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
@@ -337,8 +367,8 @@ __global__ void __launch_bounds__(256, PMAX == 1 ? 3 : 2) skinny_dot_kernel(cons
 // interleaved groups of G = VW rows of the split's K range, so every warp reads
 // whole 512-byte row segments, and their sums are added in warp order through
 // shared memory (deterministic).
-template <typename T, int PMAX>
-__global__ void __launch_bounds__(256, PMAX == 1 ? 3 : PMAX == 4 ? 2 : 1)
+template <typename T, int PMAX, bool UA>
+__global__ void __launch_bounds__(256, PMAX == 1 ? (UA ? 2 : 3) : PMAX == 4 && !UA ? 2 : 1)
     skinny_axpy_kernel(const SkinnyParams sp) {
     constexpr int VW = 16 / sizeof(T);
     constexpr int CW = 32 * VW;
@@ -370,9 +400,25 @@ __global__ void __launch_bounds__(256, PMAX == 1 ? 3 : PMAX == 4 ? 2 : 1)
         for (int64_t kb = k0 + warp * G; active && kb < k1; kb += 8 * G) {
             const int gn = static_cast<int>(min(static_cast<int64_t>(G), k1 - kb));
             uint4 raw[G];
+            if constexpr (UA) {
+                // Rows not 16-byte aligned: every row's chunk loads first (two per
+                // row), then the shifts, so that the loads are in flight together.
+                RawPair pr[G];
 #pragma unroll
-            for (int u = 0; u < G; ++u)
-                if (u < gn) raw[u] = load_raw<T, VW, true>(lcol + (kb + u) * sp.ldl, vec, nv);
+                for (int u = 0; u < G; ++u) {
+                    if (u < gn)
+                        pr[u] = load_pair<T, VW>(lcol + (kb + u) * sp.ldl, nv);
+                    else
+                        pr[u].lo = pr[u].hi = make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < G; ++u)
+                    if (u < gn) raw[u] = pair_shift<T, VW>(pr[u], lcol + (kb + u) * sp.ldl, nv);
+            } else {
+#pragma unroll
+                for (int u = 0; u < G; ++u)
+                    if (u < gn) raw[u] = load_raw<T, VW, false>(lcol + (kb + u) * sp.ldl, vec, nv);
+            }
 #pragma unroll
             for (int i = 0; i < PMAX; ++i) {
                 if (p0 + i >= sp.P) break;
@@ -499,7 +545,8 @@ cudaError_t skinny_attr_t() {
     cudaFuncAttributes fa;
     cudaError_t err = cudaFuncGetAttributes(&fa, skinny_dot_kernel<T, PM, false>);
     if (err == cudaSuccess) err = cudaFuncGetAttributes(&fa, skinny_dot_kernel<T, PM, true>);
-    if (err == cudaSuccess) err = cudaFuncGetAttributes(&fa, skinny_axpy_kernel<T, PM>);
+    if (err == cudaSuccess) err = cudaFuncGetAttributes(&fa, skinny_axpy_kernel<T, PM, false>);
+    if (err == cudaSuccess) err = cudaFuncGetAttributes(&fa, skinny_axpy_kernel<T, PM, true>);
     return err;
 }
 template <typename T>
@@ -603,7 +650,8 @@ cudaError_t launch_skinny(const gemm_config_t& cfg, const SkinnyArgs& a, const S
                (batch == 1 || (bs * es) % 16 == 0);
     };
     sp.l_vec = al16(sp.L, sp.ldl, sp.stride_l, s.batch, esz) ? 1 : 0;
-    sp.s_vec = (sp.s_sk == 1 && al16(sp.S, sp.s_sp, sp.stride_s, s.batch, esz)) ? 1 : 0;
+    // (the stride between small-operand rows matters only when there are several)
+    sp.s_vec = (sp.s_sk == 1 && al16(sp.S, sp.P > 1 ? sp.s_sp : 8, sp.stride_s, s.batch, esz)) ? 1 : 0;
     sp.e = e;
     const int sms = launch_sms(lc);
     const int pm = sp.P == 1 ? 1 : sp.P <= 4 ? 4 : 16;
@@ -632,7 +680,11 @@ cudaError_t launch_skinny(const gemm_config_t& cfg, const SkinnyArgs& a, const S
         const int vw = 16 / esz;
         const dim3 grid(static_cast<unsigned>((sp.Q + 32 * vw - 1) / (32 * vw)),
                         static_cast<unsigned>(sp.splits), static_cast<unsigned>(s.batch));
-#define G13_AXPY(T, PM) skinny_axpy_kernel<T, PM><<<grid, 256, 0, lc.stream>>>(sp)
+#define G13_AXPY(T, PM)                                                             \
+    do {                                                                            \
+        if (sp.l_vec) skinny_axpy_kernel<T, PM, false><<<grid, 256, 0, lc.stream>>>(sp); \
+        else skinny_axpy_kernel<T, PM, true><<<grid, 256, 0, lc.stream>>>(sp);           \
+    } while (0)
 #define G13_AXPY_PM(T) \
     if (pm == 1) G13_AXPY(T, 1); else if (pm == 4) G13_AXPY(T, 4); else G13_AXPY(T, 16)
         if (a.dtype == GEMM_F32) {
