@@ -1012,7 +1012,8 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                     break;
                 }
             }
-            if (EK != TC_EK_ANY || args.epi_tma) {
+            if (EK != TC_EK_ROWS && (EK != TC_EK_ANY || args.epi_tma)) {
+            if constexpr (EK != TC_EK_ROWS) {
                 if (bias_pf) {
                     // this item's bias slice (the group issued one item ago)
                     if (b_next)
@@ -1244,7 +1245,8 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                     ok = false;
                     break;
                 }
-            } else if constexpr (EK == TC_EK_ANY) {
+            }
+            } else if constexpr (EK == TC_EK_ANY || EK == TC_EK_ROWS) {
                 // C rows TMA cannot address (row stride, batch stride or base not a
                 // multiple of 16 bytes, e.g. N odd).  Each thread holds one row of a
                 // 32-row x 32-column chunk; the warp turns the chunk around in its

@@ -22,7 +22,8 @@ namespace {
 // The epilogue kind of a run: em (TMA store maps) is null when C's rows cannot
 // be stored by TMA.
 int tc_pick_ek(const EpiParams& e, const TcEpiMaps* em) {
-    if (!em || e.act == GEMM_ACT_SOFTMAX) return TC_EK_ANY;
+    if (e.act == GEMM_ACT_SOFTMAX) return TC_EK_ANY;
+    if (!em) return TC_EK_ROWS;
     if (!e.bias && e.act == GEMM_ACT_NONE && !e.R) return TC_EK_PLAIN;
     if (e.act == GEMM_ACT_GELU_ERF) return e.R ? TC_EK_ANY : TC_EK_GELU;
     return TC_EK_BIAS;

@@ -17,6 +17,9 @@ cudaError_t launch_tc_spec_nk(int ek, const gemm_config_t& cfg, int dtype, const
         if (ek == TC_EK_GELU)                                                                   \
             return launch_tc_t<BN, ST, false, EW, PAIR, false, TC_EK_GELU, false>(cfg, dtype, tmA, tmB, em,  \
                                                                           s, e, lc, fe);        \
+        if (ek == TC_EK_ROWS)                                                                   \
+            return launch_tc_t<BN, ST, false, EW, PAIR, false, TC_EK_ROWS, false>(cfg, dtype, tmA, tmB, em,  \
+                                                                          s, e, lc, fe);        \
     }
     G13_TC_SPEC_CONFIGS(G13_TC_LAUNCH)
 #undef G13_TC_LAUNCH
@@ -32,7 +35,9 @@ cudaError_t tc_preload_spec_nk() {
     if (err == cudaSuccess)                                                                        \
         err = cudaFuncGetAttributes(&fa, tc_gemm_kernel<BN, ST, false, EW, PAIR, false, TC_EK_BIAS, false>);  \
     if (err == cudaSuccess)                                                                        \
-        err = cudaFuncGetAttributes(&fa, tc_gemm_kernel<BN, ST, false, EW, PAIR, false, TC_EK_GELU, false>);
+        err = cudaFuncGetAttributes(&fa, tc_gemm_kernel<BN, ST, false, EW, PAIR, false, TC_EK_GELU, false>); \
+    if (err == cudaSuccess)                                                                        \
+        err = cudaFuncGetAttributes(&fa, tc_gemm_kernel<BN, ST, false, EW, PAIR, false, TC_EK_ROWS, false>);
     G13_TC_SPEC_CONFIGS(G13_TC_PRELOAD)
 #undef G13_TC_PRELOAD
     return err;
