@@ -92,8 +92,9 @@ constexpr int TC_VARIANT_PAIR8 = 3;
 // or without bias, no residual).  A kernel whose loop holds only the steps its
 // tiles run fetches far fewer instructions per tile.
 // TC_EK_ROWS holds only the path for C rows TMA cannot store (any epilogue but
-// the row softmax).
-constexpr int TC_EK_ANY = 0, TC_EK_PLAIN = 1, TC_EK_BIAS = 2, TC_EK_GELU = 3, TC_EK_ROWS = 4;
+// the row softmax); TC_EK_SOFTMAX only the row softmax with C stored by TMA.
+constexpr int TC_EK_ANY = 0, TC_EK_PLAIN = 1, TC_EK_BIAS = 2, TC_EK_GELU = 3, TC_EK_ROWS = 4,
+              TC_EK_SOFTMAX = 5;
 // The launchers of each part (tc_any_*.cu, tc_spec_*.cu, tc_sk_*.cu); the spec
 // ones take the kind, and the spec and stream-K ones the configurations of
 // tc_has_spec only.

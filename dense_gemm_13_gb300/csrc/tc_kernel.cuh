@@ -943,7 +943,7 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                 }
                 return xb[(ew ^ 4) * 32 + lane];
             };
-            if (EK == TC_EK_ANY && e.act == GEMM_ACT_SOFTMAX) {
+            if ((EK == TC_EK_ANY || EK == TC_EK_SOFTMAX) && e.act == GEMM_ACT_SOFTMAX) {
                 constexpr float LOG2E = 1.4426950408889634f;
                 const float a2 = e.alpha * LOG2E;
                 // valid columns in this warp's slice (int32: at most SLICE)
@@ -1101,7 +1101,7 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                         return true;
                     }
                     float y[32];
-                    const bool smx = KIND == 4 && e.act == GEMM_ACT_SOFTMAX;  // v holds exp(t - max)
+                    const bool smx = (KIND == 4 || EK == TC_EK_SOFTMAX) && e.act == GEMM_ACT_SOFTMAX;  // v: exp(t - max)
                     if (KIND == 0 || (KIND == 4 && (args.epi_plain || smx))) {
                         const float sc = smx ? sinv : e.alpha;
 #pragma unroll
@@ -1235,7 +1235,7 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                 return true;
                 };
                 const auto run_kind = [&](auto w_tag) -> bool {
-                    constexpr int KIND = EK == TC_EK_PLAIN ? 0 : EK == TC_EK_BIAS ? 1
+                    constexpr int KIND = EK == TC_EK_PLAIN || EK == TC_EK_SOFTMAX ? 0 : EK == TC_EK_BIAS ? 1
                                          : EK == TC_EK_GELU ? 3 : 4;
                     return chunk_loop(w_tag, std::integral_constant<int, KIND>{});
                 };
@@ -1594,6 +1594,12 @@ cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& 
     X(128, 4, 8, 1, false)     \
     X(256, 6, 4, 2, true)      \
     X(256, 5, 8, 3, true)
+
+// The configurations the dispatcher picks for the row softmax, which also come
+// as kernels holding only the softmax epilogue (TC_EK_SOFTMAX).
+#define G13_TC_SOFTMAX_CONFIGS(X) \
+    X(256, 3, 8, 1, false)        \
+    X(512, 1, 8, 1, false)
 
 // 3xTF32 configurations: (BN, STAGES, epilogue warps, variant, pair); 64 KB stages.
 #define G13_TC3_CONFIGS(X)   \

@@ -19,10 +19,18 @@ bool tc_has_spec(const gemm_config_t& cfg) {
 
 namespace {
 
+bool tc_has_softmax(const gemm_config_t& cfg) {
+#define G13_TC_HAS(BN, ST, EW, VAR, PAIR) \
+    if (cfg.bn == BN && cfg.stages == ST && cfg.variant == VAR) return true;
+    G13_TC_SOFTMAX_CONFIGS(G13_TC_HAS)
+#undef G13_TC_HAS
+    return false;
+}
+
 // The epilogue kind of a run: em (TMA store maps) is null when C's rows cannot
 // be stored by TMA.
 int tc_pick_ek(const EpiParams& e, const TcEpiMaps* em) {
-    if (e.act == GEMM_ACT_SOFTMAX) return TC_EK_ANY;
+    if (e.act == GEMM_ACT_SOFTMAX) return em ? TC_EK_SOFTMAX : TC_EK_ANY;
     if (!em) return TC_EK_ROWS;
     if (!e.bias && e.act == GEMM_ACT_NONE && !e.R) return TC_EK_PLAIN;
     if (e.act == GEMM_ACT_GELU_ERF) return e.R ? TC_EK_ANY : TC_EK_GELU;
@@ -68,7 +76,10 @@ cudaError_t launch_tc(const gemm_config_t& cfg, int dtype, int b_layout, const C
                   : launch_tc_sk_nk(cfg, dtype, tmA, tmB, em, s, e, lc, final_epi);
     }
     const int ek = tc_pick_ek(e, em);
-    if (ek != TC_EK_ANY && tc_has_spec(cfg))
+    if (ek == TC_EK_SOFTMAX && tc_has_softmax(cfg))
+        return kn ? launch_tc_spec_kn(ek, cfg, dtype, tmA, tmB, em, s, e, lc, final_epi)
+                  : launch_tc_spec_nk(ek, cfg, dtype, tmA, tmB, em, s, e, lc, final_epi);
+    if (ek != TC_EK_ANY && ek != TC_EK_SOFTMAX && tc_has_spec(cfg))
         return kn ? launch_tc_spec_kn(ek, cfg, dtype, tmA, tmB, em, s, e, lc, final_epi)
                   : launch_tc_spec_nk(ek, cfg, dtype, tmA, tmB, em, s, e, lc, final_epi);
     return kn ? launch_tc_any_kn(cfg, dtype, tmA, tmB, em, s, e, lc, final_epi)

@@ -23,6 +23,12 @@ cudaError_t launch_tc_spec_kn(int ek, const gemm_config_t& cfg, int dtype, const
     }
     G13_TC_SPEC_CONFIGS(G13_TC_LAUNCH)
 #undef G13_TC_LAUNCH
+#define G13_TC_LAUNCH_SMX(BN, ST, EW, VAR, PAIR)                                                \
+    if (ek == TC_EK_SOFTMAX && cfg.bn == BN && cfg.stages == ST && cfg.variant == VAR)         \
+        return launch_tc_t<BN, ST, true, EW, PAIR, false, TC_EK_SOFTMAX, false>(cfg, dtype, tmA, tmB,  \
+                                                                            em, s, e, lc, fe);
+    G13_TC_SOFTMAX_CONFIGS(G13_TC_LAUNCH_SMX)
+#undef G13_TC_LAUNCH_SMX
     return cudaErrorInvalidValue;
 }
 
@@ -40,6 +46,11 @@ cudaError_t tc_preload_spec_kn() {
         err = cudaFuncGetAttributes(&fa, tc_gemm_kernel<BN, ST, true, EW, PAIR, false, TC_EK_ROWS, false>);
     G13_TC_SPEC_CONFIGS(G13_TC_PRELOAD)
 #undef G13_TC_PRELOAD
+#define G13_TC_PRELOAD_SMX(BN, ST, EW, VAR, PAIR)                                                   \
+    if (err == cudaSuccess)                                                                         \
+        err = cudaFuncGetAttributes(&fa, tc_gemm_kernel<BN, ST, true, EW, PAIR, false, TC_EK_SOFTMAX, false>);
+    G13_TC_SOFTMAX_CONFIGS(G13_TC_PRELOAD_SMX)
+#undef G13_TC_PRELOAD_SMX
     return err;
 }
 
