@@ -26,6 +26,7 @@
 
 #include "epilogue.cuh"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace g13 {
 namespace {
@@ -61,35 +62,47 @@ __device__ __forceinline__ uint4 window16(const uint4& lo, const uint4& hi, int 
 // up to dst_ld) get whatever the last source piece holds there; the GEMM's
 // tensor maps end at the row's last column and never read them.
 constexpr int STAGE_PIECES = 4;  // per lane per unit
-__global__ void stage_copy_kernel(const uint8_t* __restrict__ src, int64_t rows, int64_t row_bytes,
-                                  int64_t ld_bytes, int64_t bstride_bytes, int64_t batch,
-                                  uint8_t* __restrict__ dst, int64_t dst_ld_bytes) {
+struct StageArgs {
+    const uint8_t* src;
+    int64_t rows, row_bytes, ld_bytes, bstride_bytes, batch;
+    uint8_t* dst;
+    int64_t dst_ld_bytes;
+    int64_t units;  // work units of this job
+};
+// Up to two jobs (both operands of a GEMM) in one launch: units of job 0, then of job 1.
+__global__ void stage_copy_kernel(const StageArgs j0, const StageArgs j1, int njobs) {
+    // the GEMM launched after this copy may start its set-up now; it waits for
+    // this grid to finish before reading the copies
+    griddep_launch();
     const int lane = threadIdx.x & 31;
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-    const int64_t npiece = (row_bytes + 15) / 16;
-    const int64_t per_row = (npiece + 32 * STAGE_PIECES - 1) / (32 * STAGE_PIECES);
-    const int64_t units = rows * batch * per_row;
-    for (int64_t u = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-         u < units; u += warps) {
+    const int64_t units = j0.units + (njobs > 1 ? j1.units : 0);
+    for (int64_t uu = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+         uu < units; uu += warps) {
+        const bool second = uu >= j0.units;
+        const StageArgs& J = second ? j1 : j0;
+        const int64_t u = second ? uu - j0.units : uu;
+        const int64_t npiece = (J.row_bytes + 15) / 16;
+        const int64_t per_row = (npiece + 32 * STAGE_PIECES - 1) / (32 * STAGE_PIECES);
         const int64_t r = u / per_row;
-        const int64_t j0 = (u - r * per_row) * (32 * STAGE_PIECES) + lane;
-        const int64_t b = r / rows, i = r - b * rows;
-        const uintptr_t a = reinterpret_cast<uintptr_t>(src + b * bstride_bytes + i * ld_bytes);
+        const int64_t j0p = (u - r * per_row) * (32 * STAGE_PIECES) + lane;
+        const int64_t b = r / J.rows, i = r - b * J.rows;
+        const uintptr_t a = reinterpret_cast<uintptr_t>(J.src + b * J.bstride_bytes + i * J.ld_bytes);
         const int sh = static_cast<int>(a & 15);
         const uint4* base = reinterpret_cast<const uint4*>(a - sh);
-        uint4* d = reinterpret_cast<uint4*>(dst + r * dst_ld_bytes);
+        uint4* d = reinterpret_cast<uint4*>(J.dst + r * J.dst_ld_bytes);
         uint4 lo[STAGE_PIECES], hi[STAGE_PIECES];
 #pragma unroll
         for (int q = 0; q < STAGE_PIECES; ++q) {
-            const int64_t j = j0 + 32 * q;
-            const int64_t left = row_bytes - 16 * j;  // wanted bytes from piece j on
+            const int64_t j = j0p + 32 * q;
+            const int64_t left = J.row_bytes - 16 * j;  // wanted bytes from piece j on
             lo[q] = j < npiece ? __ldg(base + j) : make_uint4(0, 0, 0, 0);
             hi[q] = j < npiece && sh + (left < 16 ? left : 16) > 16 ? __ldg(base + j + 1)
                                                                    : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int q = 0; q < STAGE_PIECES; ++q) {
-            const int64_t j = j0 + 32 * q;
+            const int64_t j = j0p + 32 * q;
             if (j < npiece) d[j] = window16(lo[q], hi[q], sh);
         }
     }
@@ -578,22 +591,41 @@ cudaError_t aux_preload_kernels() {
     return err;
 }
 
+cudaError_t launch_stage_copies(const StageJob* jobs, int njobs, int esz, cudaStream_t stream) {
+    StageArgs a[2] = {};
+    int n = 0;
+    for (int k = 0; k < njobs && k < 2; ++k) {
+        const StageJob& J = jobs[k];
+        const int64_t total = J.rows * J.batch;
+        if (total <= 0 || J.cols <= 0) continue;
+        if (reinterpret_cast<uintptr_t>(J.dst) % 16 != 0 || (J.dst_ld * esz) % 16 != 0)
+            return cudaErrorInvalidValue;
+        const int64_t npiece = (J.cols * esz + 15) / 16;
+        a[n].src = static_cast<const uint8_t*>(J.src);
+        a[n].rows = J.rows;
+        a[n].row_bytes = J.cols * esz;
+        a[n].ld_bytes = J.ld * esz;
+        a[n].bstride_bytes = J.bstride * esz;
+        a[n].batch = J.batch;
+        a[n].dst = static_cast<uint8_t*>(J.dst);
+        a[n].dst_ld_bytes = J.dst_ld * esz;
+        a[n].units = total * ((npiece + 127) / 128);
+        ++n;
+    }
+    if (n == 0) return cudaSuccess;
+    // 8 warps per block, at most 8 blocks per SM's worth of work units
+    const int64_t units = a[0].units + (n > 1 ? a[1].units : 0);
+    const int64_t blocks = (units + 7) / 8;
+    const unsigned grid = static_cast<unsigned>(blocks < 152 * 8 ? blocks : 152 * 8);
+    stage_copy_kernel<<<grid, 256, 0, stream>>>(a[0], a[1], n);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_stage_copy(const void* src, int64_t rows, int64_t cols, int64_t ld,
                               int64_t bstride, int64_t batch, int esz, void* dst, int64_t dst_ld,
                               cudaStream_t stream) {
-    const int64_t total = rows * batch;
-    if (total <= 0 || cols <= 0) return cudaSuccess;
-    if (reinterpret_cast<uintptr_t>(dst) % 16 != 0 || (dst_ld * esz) % 16 != 0)
-        return cudaErrorInvalidValue;
-    // 8 warps per block, at most 8 blocks per SM's worth of work units
-    const int64_t npiece = (cols * esz + 15) / 16;
-    const int64_t units = total * ((npiece + 127) / 128);
-    const int64_t blocks = (units + 7) / 8;
-    const unsigned grid = static_cast<unsigned>(blocks < 152 * 8 ? blocks : 152 * 8);
-    stage_copy_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint8_t*>(src), rows, cols * esz,
-                                                ld * esz, bstride * esz, batch,
-                                                static_cast<uint8_t*>(dst), dst_ld * esz);
-    return cudaGetLastError();
+    const StageJob j{src, rows, cols, ld, bstride, batch, dst, dst_ld};
+    return launch_stage_copies(&j, 1, esz, stream);
 }
 
 void skinny_geometry(int64_t M, int64_t N, int b_layout, int64_t* P, int64_t* Q, int* dot) {

@@ -492,22 +492,29 @@ int gemm_run(gemm_plan_t plan, const void* A, const void* B, void* C, const void
     int64_t sa = ga.bstride, sb = gb.bstride;
     if (reinterpret_cast<uintptr_t>(A) % 16 != 0 && !cfg.stage_a) return GEMM_ERR_MISALIGNED;
     if (reinterpret_cast<uintptr_t>(B) % 16 != 0 && !cfg.stage_b) return GEMM_ERR_MISALIGNED;
+    // The staging copies of both operands go out as one launch.
+    StageJob jobs[2];
+    int njobs = 0;
     if (cfg.stage_a) {
-        ce = launch_stage_copy(A, ga.rows, ga.cols, ga.ld, ga.bstride, ga.batches, esz, plan->d_ws,
-                               plan->lda_s, st);
-        if (ce != cudaSuccess) return map_cuda_error(ce);
+        jobs[njobs++] = StageJob{A, ga.rows, ga.cols, ga.ld, ga.bstride, ga.batches, plan->d_ws,
+                                 plan->lda_s};
         a_src = plan->d_ws;
         lda = plan->lda_s;
         sa = plan->stride_as;
     }
     if (cfg.stage_b) {
         void* dst = static_cast<char*>(plan->d_ws) + plan->ws_b_off;
-        ce = launch_stage_copy(B, gb.rows, gb.cols, gb.ld, gb.bstride, gb.batches, esz, dst,
-                               plan->ldb_s, st);
-        if (ce != cudaSuccess) return map_cuda_error(ce);
+        jobs[njobs++] = StageJob{B, gb.rows, gb.cols, gb.ld, gb.bstride, gb.batches, dst, plan->ldb_s};
         b_src = dst;
         ldb = plan->ldb_s;
         sb = plan->stride_bs;
+    }
+    if (njobs) {
+        ce = launch_stage_copies(jobs, njobs, esz, st);
+        if (ce != cudaSuccess) return map_cuda_error(ce);
+        // the tensor-core kernel may start while the copy finishes (it waits for
+        // the copy before its first operand load)
+        lc.pdl = cfg.kernel == GEMM_KERNEL_TC ? 1 : 0;
     }
     s.a_bmul = ga.batches > 1 ? 1 : 0;
     s.b_bmul = gb.batches > 1 ? 1 : 0;

@@ -40,6 +40,9 @@ struct LaunchCtx {
     unsigned* sk_tags;
     int64_t sk_grid;
     unsigned sk_epoch;
+    // the kernel is launched as a programmatic dependent of the staging copy just
+    // before it in the stream (it waits for the copy before its first load)
+    int pdl;
 };
 
 // TMA descriptors for the tensor-core epilogue: C (box of 32 rows x 128 bytes,
@@ -205,6 +208,16 @@ int tmap_encode_3d(CUtensorMap* m, int dtype, const void* base, int64_t cols, in
 // size esz) into a dense [batch][rows][dst_ld] buffer (dst and dst_ld * esz
 // multiples of 16 bytes, else cudaErrorInvalidValue).  Padding columns get
 // unspecified bytes: the tensor maps over the copy end at column cols.
+// One staging copy job: rows x cols elements of esz bytes (row stride ld,
+// batch stride bstride, batch batches) into dst with row stride dst_ld.
+struct StageJob {
+    const void* src;
+    int64_t rows, cols, ld, bstride, batch;
+    void* dst;
+    int64_t dst_ld;
+};
+// Both operands' staging copies in one launch (njobs 1 or 2).
+cudaError_t launch_stage_copies(const StageJob* jobs, int njobs, int esz, cudaStream_t stream);
 cudaError_t launch_stage_copy(const void* src, int64_t rows, int64_t cols, int64_t ld,
                               int64_t bstride, int64_t batch, int esz, void* dst,
                               int64_t dst_ld, cudaStream_t stream);

@@ -120,6 +120,18 @@ __device__ __forceinline__ void cp_async_16z(uint32_t dst, const void* src, uint
                  "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
                  : "memory");
 }
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start while the kernel before it in the
+// stream finishes; griddep_wait blocks until that kernel has completed and its
+// memory is visible (a no-op without such a predecessor); griddep_launch lets
+// the dependent kernel start early.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Release store / acquire load of a flag in global memory, at GPU scope.
 __device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");

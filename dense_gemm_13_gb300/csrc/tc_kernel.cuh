@@ -405,6 +405,9 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
             uint32_t ph = 0;
             uint32_t armed = 0, armed_par = 0;  // per stage: armed and not yet seen consumed
             bool ok = true;
+            // A staging copy launched just before this kernel (programmatic
+            // dependent launch) must have finished before the first operand load.
+            griddep_wait();
             for (int64_t cur = w_begin; ok && cur < w_end;) {
                 const bool first_it = cur == w_begin;
                 const TcItem it = tc_item<SK>(args, cur, w_stride, w_end, holder);
@@ -1502,6 +1505,8 @@ cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& 
         lcfg.dynamicSmemBytes = smem;
         lcfg.stream = lc.stream;
         cudaLaunchAttribute attr[2];
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
@@ -1529,8 +1534,9 @@ cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& 
             tc_sk_split(a, pairs);
             attr[1] = coop;
             lcfg.numAttrs = 2;
-        } else if (pairs > a.total_items) {
-            pairs = a.total_items;
+        } else {
+            if (pairs > a.total_items) pairs = a.total_items;
+            if (lc.pdl) lcfg.numAttrs = 2;  // programmatic dependent of the staging copy
         }
         if (pairs < 1) pairs = 1;
         lcfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
@@ -1561,8 +1567,23 @@ cudaError_t launch_tc_t(const gemm_config_t& cfg, int dtype, const CUtensorMap& 
         lcfg.numAttrs = 1;
         return cudaLaunchKernelEx(&lcfg, kern, tmA, tmB, mc, mr, a);
     }
-    kern<<<static_cast<unsigned>(grid), tc_threads<EW>(), smem, lc.stream>>>(tmA, tmB, mc, mr, a);
-    err2 = cudaGetLastError();
+    if (lc.pdl) {
+        // a programmatic dependent of the staging copy just before it
+        cudaLaunchConfig_t lcfg = {};
+        lcfg.gridDim = dim3(static_cast<unsigned>(grid));
+        lcfg.blockDim = dim3(tc_threads<EW>());
+        lcfg.dynamicSmemBytes = smem;
+        lcfg.stream = lc.stream;
+        cudaLaunchAttribute pdl;
+        pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        pdl.val.programmaticStreamSerializationAllowed = 1;
+        lcfg.attrs = &pdl;
+        lcfg.numAttrs = 1;
+        err2 = cudaLaunchKernelEx(&lcfg, kern, tmA, tmB, mc, mr, a);
+    } else {
+        kern<<<static_cast<unsigned>(grid), tc_threads<EW>(), smem, lc.stream>>>(tmA, tmB, mc, mr, a);
+        err2 = cudaGetLastError();
+    }
     if (err2 != cudaSuccess || a.splits == 1) return err2;
     // split-K: add the partial slabs in split order and apply the real epilogue
     return launch_split_reduce(static_cast<const float*>(e.C), s.M, s.N, s.batch, a.splits,
