@@ -497,6 +497,7 @@ __global__ void __launch_bounds__(256, PMAX == 1 ? (UA ? 2 : 3) : PMAX == 4 && !
 __global__ void __launch_bounds__(256) split_reduce_kernel(const float* __restrict__ partial,
                                                            int64_t M, int64_t N, int64_t batch,
                                                            int splits, int vec, EpiParams e) {
+    griddep_wait();  // launched as a programmatic dependent of the GEMM writing the partials
     const int64_t nq = (N + 3) / 4;
     const int64_t total = batch * M * nq;
     const int64_t slab = M * N;
@@ -753,6 +754,7 @@ __global__ void __launch_bounds__(256) tf32_split_rows_kernel(const float* __res
                                                               int64_t batches, int vec,
                                                               float* __restrict__ out,
                                                               int64_t ldo) {
+    griddep_launch();  // the tensor-core GEMM after this pass may start its set-up
     const int64_t q = ldo / 4;  // 4-column groups per output row
     const int64_t total = batches * rows * q;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -789,6 +791,7 @@ __global__ void __launch_bounds__(256) tf32_split_transpose_kernel(
     const float* __restrict__ X, int64_t rows, int64_t cols, int64_t ld, int64_t bstride,
     int64_t batches, float* __restrict__ out, int64_t ldo) {
     __shared__ float t[32][33];
+    griddep_launch();  // the tensor-core GEMM after this pass may start its set-up
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
     const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 32;
     const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 32;
@@ -889,9 +892,18 @@ cudaError_t launch_split_reduce(const float* partial, int64_t M, int64_t N, int6
     int64_t rb = (quads + 255) / 256;
     if (rb > static_cast<int64_t>(sms) * 16) rb = static_cast<int64_t>(sms) * 16;
     const int vec = (N % 4 == 0 && reinterpret_cast<uintptr_t>(partial) % 16 == 0) ? 1 : 0;
-    split_reduce_kernel<<<static_cast<unsigned>(rb), 256, 0, lc.stream>>>(partial, M, N, batch,
-                                                                          splits, vec, e);
-    return cudaGetLastError();
+    // a programmatic dependent of the GEMM that writes the partials (it waits for
+    // that grid before reading them), so its launch overlaps the GEMM's tail
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(rb));
+    cfg.blockDim = dim3(256);
+    cfg.stream = lc.stream;
+    cudaLaunchAttribute pdl;
+    pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &pdl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, split_reduce_kernel, partial, M, N, batch, splits, vec, e);
 }
 
 }  // namespace g13

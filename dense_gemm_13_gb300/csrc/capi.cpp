@@ -466,6 +466,7 @@ int gemm_run(gemm_plan_t plan, const void* A, const void* B, void* C, const void
             ce = launch_tf32_split(static_cast<const float*>(B), gb.rows, gb.cols, gb.ld,
                                    gb.bstride, gb.batches, ep.b_layout == GEMM_B_KN, wb, ldt, st);
         if (ce != cudaSuccess) return map_cuda_error(ce);
+        lc.pdl = 1;  // the GEMM starts as a programmatic dependent of the split pass
         s.a_bmul = ga.batches > 1 ? 1 : 0;
         s.b_bmul = gb.batches > 1 ? 1 : 0;
         std::lock_guard<std::mutex> lk(plan->mu);

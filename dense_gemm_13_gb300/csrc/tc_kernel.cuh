@@ -362,6 +362,9 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
     const int64_t w_stride = n_holders;
 
     if (warp == 0 && lane == 0) {
+        // a kernel launched after this one as its programmatic dependent (the
+        // split-K reduction) may start; it waits for this grid before its reads
+        griddep_launch();
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
