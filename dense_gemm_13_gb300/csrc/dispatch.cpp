@@ -168,7 +168,9 @@ int tc_splits(const Problem& p, int num_sms, int bn) {
         const double t_mem = (rows + cols) * kpart * esz / share;
         const double waves = static_cast<double>(cdiv(items, num_sms));
         double t = waves * std::max(t_mma, t_mem);
-        if (s > 1) t += static_cast<double>(s) * M * N * bt * 8.0 / 6e12 + 4e-6;
+        // the reduction pass: its slab traffic and ~2 us (its launch overlaps the
+        // GEMM's tail as a programmatic dependent)
+        if (s > 1) t += static_cast<double>(s) * M * N * bt * 8.0 / 6e12 + 2e-6;
         return t;
     };
     int best = 1;
