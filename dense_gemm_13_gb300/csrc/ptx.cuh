@@ -103,6 +103,11 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// Hint: bring the global-memory line holding `p` into L2 (no data returned,
+// no register written).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
 // 4-byte asynchronous copy from global to shared memory; with `pred` false
 // nothing is read and the destination is zero-filled (src must still be a
 // valid address).

@@ -693,6 +693,28 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                 epi0_lt = 1;
             }
         }
+        // C rows TMA cannot address: the four-byte residual copies of the per-row
+        // path wait on DRAM one chunk at a time, so with a short main loop (K of
+        // at most 8 blocks: the epilogue is the kernel's work) the warp asks L2
+        // for its rows of a work item's residual an item ahead (the first item's
+        // at the start).  With longer K the requests compete with the operand
+        // loads and cost more than they save.
+        const bool r_pf = (EK == TC_EK_ANY || EK == TC_EK_ROWS) && !args.epi_tma &&
+                          args.k_blocks <= 8 && e.R != nullptr && !args.epi_plain &&
+                          e.act != GEMM_ACT_SOFTMAX;
+        const auto r_prefetch = [&](int64_t tile) {
+            int64_t bidx, mt2, nt2;
+            tc_tile_coords(tile, args, bidx, mt2, nt2);
+            const int64_t r = mt2 * L::TILE_M + rank * TBM + q * 32 + lane;
+            const int64_t c0 = nt2 * BN + c_lo;
+            if (r >= e.M || c0 >= e.N) return;
+            const int64_t n = min(int64_t(SLICE), e.N - c0);
+            const float* p = e.R + bidx * e.stride_r + r * e.ldr + c0;
+            // one element per 128-byte line of the row segment, and its last
+            for (int64_t i = 0; i < n; i += 32) prefetch_l2(p + i);
+            prefetch_l2(p + n - 1);
+        };
+        if (r_pf && epi0_tile >= 0) r_prefetch(epi0_tile);
         if (args.r_ahead && epi0_tile >= 0) {
             int32_t cg, r0, bidx;
             if (first_chunk(epi0_tile, cg, r0, bidx)) {
@@ -750,6 +772,10 @@ __global__ void __launch_bounds__(tc_threads<EW>(), 1)
                 }
                 return false;
             };
+            if (r_pf) {
+                int64_t ntile;
+                if (next_epi_tile(ntile)) r_prefetch(ntile);
+            }
             const int buf = NBUF == 1 ? 0 : (lt & 1);
             const uint32_t tph = static_cast<uint32_t>(NBUF == 1 ? lt : (lt >> 1)) & 1u;
             const bool b_next = bias_pf && has_nx && lt + 1 > epi0_lt;
