@@ -333,6 +333,35 @@ int choose_config(const Problem& p, int num_sms, gemm_config_t* out) {
                 }
             }
         }
+        // Short K with C rows TMA can store: when a tile's main loop outlasts its
+        // epilogue, CTA pairs with eight epilogue warps (5 stages) run the main
+        // loop ~17 % faster than single CTAs and keep the 8-warp epilogue.  Clock64
+        // traces on GB300: a 128 x 256 x 64 block takes ~700 cycles on a single
+        // CTA; the epilogue of a 128 x 256 tile ~4.5 K cycles plain, ~9 K with
+        // bias + GELU, ~8 K with an FP32 residual.  Measured (L2 flushed, us,
+        // single -> pairs): 4096^2 x 768 BF16 out 33.3 -> 30.4, 8192^2 x 1024
+        // 111.3 -> 92.3, 4096^2 x 1024 bias + GELU 42.1 -> 39.6, 6144^2 x 1000
+        // + FP32 residual 99.6 -> 88.1; FFN1 (4096 x 3072 x 768, bias + GELU)
+        // stays single: 29.4 vs 32.0 with pairs.
+        const int osz = dtype_size(p.epi.out_dtype);
+        const bool c_tma = (p.ldc * osz) % 16 == 0 && (bt == 1 || (p.epi.stride_c * osz) % 16 == 0);
+        if (c.split_k == 1 && K <= 1024 && num_sms >= 2 && c_tma) {
+            int64_t epi_cycles = 4500;
+            if (p.epi.act == GEMM_ACT_GELU_ERF) epi_cycles += 4500;
+            if (p.epi.has_residual) epi_cycles += 3500;
+            if (cdiv(K, 64) * 700 > epi_cycles) {
+                const int64_t pair_waves = cdiv(bt * cdiv(M, 256) * cdiv(N, 256), num_sms / 2);
+                const int64_t cost_single =
+                    (c.bn == 128 ? waves128 * 128 * 5 : waves256 * 256 * 4) * 100;
+                const int64_t cost_pair = pair_waves * 256 * 4 * 85;
+                if (cost_pair < cost_single) {
+                    c.bn = 256;
+                    c.stages = 5;
+                    c.variant = TC_VARIANT_PAIR8;
+                    c.raster_group = static_cast<int32_t>(std::min<int64_t>(16, cdiv(M, 256)));
+                }
+            }
+        }
     }
     set_staging(p, &c);
     *out = c;

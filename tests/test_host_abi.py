@@ -118,8 +118,14 @@ def test_dispatch_buckets(lib):
     assert sel("f32", 256, 256, 256).kernel == "ffma"
     c = sel("bf16", 8192, 8192, 8192, "nk")
     assert (c.kernel, c.bm, c.bn, c.bk, c.variant, c.stages) == ("tc", 128, 256, 64, 2, 6)  # pairs
+    c = sel("f16", 4096, 3072, 768, "nk", bias=True, act="gelu", out_dtype="bf16")
+    assert (c.kernel, c.variant, c.stages) == ("tc", 1, 3)   # short K, heavy epilogue: 8 warps
     c = sel("f16", 4096, 3072, 768, "nk")
-    assert (c.kernel, c.variant, c.stages) == ("tc", 1, 3)   # short K: 8 epilogue warps
+    assert (c.kernel, c.variant, c.stages) == ("tc", 3, 5)   # main loop outlasts a plain epilogue
+    c = sel("bf16", 6144, 6144, 1000, residual=True)
+    assert (c.kernel, c.variant, c.stages) == ("tc", 3, 5)   # ... and an FP32 residual
+    assert sel("bf16", 6144, 6144, 127, residual=True).variant == 1   # 2 K blocks: epilogue-bound
+    assert sel("bf16", 6144, 4097, 1000, residual=True).variant == 1  # rows TMA cannot store
     c = sel("bf16", 4096, 768, 3072, "kn")
     assert (c.kernel, c.variant) == ("tc", 2)                # 48 pair tiles: one wave of pairs
     c = sel("bf16", 256, 256, 4096, "nk")
