@@ -126,6 +126,13 @@ def test_dispatch_buckets(lib):
     assert (c.kernel, c.variant, c.stages) == ("tc", 3, 5)   # ... and an FP32 residual
     assert sel("bf16", 6144, 6144, 127, residual=True).variant == 1   # 2 K blocks: epilogue-bound
     assert sel("bf16", 6144, 4097, 1000, residual=True).variant == 1  # rows TMA cannot store
+    # the short-K pair rule's epilogue weights: bias + GELU over 16 K blocks still pairs,
+    # GELU with a residual never does for K <= 1024, nor one wave of single tiles
+    assert sel("bf16", 4096, 4096, 1024, "nk", bias=True, act="gelu").variant == 3
+    assert sel("bf16", 4096, 4096, 1024, "nk", bias=True, act="gelu", residual=True).variant == 1
+    assert sel("bf16", 4096, 4096, 512, "nk", bias=True).variant == 3
+    assert sel("bf16", 4096, 4096, 384, "nk").variant == 1             # 6 K blocks: epilogue-bound
+    assert sel("bf16", 4096, 4096, 1024, "nk", sms=1).variant == 1     # a pair needs two SMs
     c = sel("bf16", 4096, 768, 3072, "kn")
     assert (c.kernel, c.variant) == ("tc", 2)                # 48 pair tiles: one wave of pairs
     c = sel("bf16", 256, 256, 4096, "nk")
